@@ -1,0 +1,399 @@
+"""Pins for the CPU oracle against things other than itself.
+
+Each test checks an oracle function against a library routine, a textbook
+formula written differently, a hand-worked example, a closed form printed on
+the pages, or an invariant -- chosen so that a dropped term, a wrong sign or
+index, or a transposed operand fails one of them.  CPU only.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def f32(x):
+    return np.float32(x)
+
+
+def next_up(x):
+    return np.nextafter(np.float32(x), np.float32(np.inf))
+
+
+def next_down(x):
+    return np.nextafter(np.float32(x), np.float32(-np.inf))
+
+
+def rne_to_grid(a: np.ndarray, mant_bits: int, emin: int) -> np.ndarray:
+    """Textbook round-to-nearest-even of |a| to a binary format with
+    `mant_bits` fraction bits and minimum normal exponent emin, unbounded
+    above: quantum = 2^(max(floor(log2 a), emin) - mant_bits), then np.rint
+    (ties to even) on a / quantum."""
+    a = np.abs(a.astype(np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, emin)
+    quantum = np.exp2(e - mant_bits)
+    return np.rint(a / quantum) * quantum
+
+
+# ----------------------------------------------------------- code tables ---
+
+def test_e4m3_values_match_torch_float8():
+    """All 256 E4M3FN codes decode to what torch's float8_e4m3fn decodes."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3_value(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_e2m1_values_characterised():
+    """E2M1 magnitudes are exactly the numbers v <= 6 with 2v integral and at
+    most two significant bits, i.e. {0, .5, 1, 1.5, 2, 3, 4, 6}; the sign is
+    bit 3; every value is exact in E4M3 (torch round trip)."""
+    mags = [oracle.e2m1_value(c) for c in range(8)]
+    cand = sorted({v / 2 for v in range(0, 13)
+                   if v == 0 or bin(v).strip("0b").rstrip("0").__len__() <= 2})
+    assert mags == cand == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(8):
+        assert oracle.e2m1_value(c | 8) == -mags[c]
+        assert math.copysign(1.0, oracle.e2m1_value(c | 8)) == -1.0
+    t = torch.tensor(mags, dtype=torch.float32)
+    assert torch.equal(t.to(torch.float8_e4m3fn).to(torch.float32), t)
+
+
+def _probe_points(values, lo_clip, hi_clip):
+    """Each representable value and each midpoint between neighbours, plus one
+    binary32 ulp either side of it."""
+    vals = sorted(set(values))
+    pts = []
+    for i, v in enumerate(vals):
+        pts.append(v)
+        if i + 1 < len(vals):
+            m = (v + vals[i + 1]) / 2
+            pts += [m]
+    out = []
+    for p in pts:
+        p = f32(p)
+        out += [p, next_up(p), next_down(p)]
+    out = np.array([x for x in out if lo_clip <= x <= hi_clip], dtype=np.float32)
+    return out
+
+
+def test_e4m3_encode_matches_torch_cast():
+    """RNE into E4M3FN equals torch's float -> float8_e4m3fn cast on every
+    code, every midpoint (+-1 ulp) and 200k log-uniform samples up to 448."""
+    mags = [oracle.e4m3_value(c) for c in range(0x7F)]
+    pts = _probe_points(mags, 0.0, 448.0)
+    rng = np.random.default_rng(1)
+    rnd = np.exp2(rng.uniform(-14, math.log2(448.0), 200_000)).astype(np.float32)
+    x = np.concatenate([pts, rnd, -pts, -rnd])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([oracle.e4m3_encode(v) for v in x], dtype=np.uint8)
+    bad = np.nonzero(ref != ours)[0]
+    assert bad.size == 0, [(float(x[i]), hex(ref[i]), hex(ours[i])) for i in bad[:10]]
+
+
+def test_e4m3_encode_saturates_and_specials():
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(463.9) == 0x7E
+    assert oracle.e4m3_encode(1e30) == 0x7E        # satfinite, not NaN
+    assert oracle.e4m3_encode(float("inf")) == 0x7E
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00  # tie between 0 and 2^-9 -> even code 0
+    assert oracle.e4m3_encode(float(next_up(2.0 ** -10))) == 0x01
+    assert oracle.e4m3_encode(0.0) == 0x00
+
+
+def test_e2m1_encode_matches_textbook_rne():
+    """RNE into E2M1 equals the textbook rounding to 1 fraction bit with
+    emin = 0 (subnormal quantum 0.5), saturated at 6."""
+    mags = [oracle.e2m1_value(c) for c in range(8)]
+    pts = _probe_points(mags + [8.0], 0.0, 7.5)
+    rng = np.random.default_rng(2)
+    rnd = np.exp2(rng.uniform(-6, 3, 100_000)).astype(np.float32)
+    x = np.concatenate([pts, rnd])
+    val = np.minimum(rne_to_grid(x, 1, 0), 6.0)
+    lookup = {m: c for c, m in enumerate(mags)}
+    for sgn in (1.0, -1.0):
+        xs = (sgn * x).astype(np.float32)
+        ours = np.array([oracle.e2m1_encode(v) for v in xs])
+        ref = np.array([lookup[v] for v in val]) | (8 if sgn < 0 else 0)
+        bad = np.nonzero(ours != ref)[0]
+        assert bad.size == 0, [(float(xs[i]), ours[i], ref[i]) for i in bad[:10]]
+
+
+def test_e2m1_encode_hand_ties_and_signed_zero():
+    cases = [(0.25, 0x0), (0.75, 0x2), (1.25, 0x2), (1.75, 0x4), (2.5, 0x4), (3.5, 0x6),
+             (5.0, 0x6), (6.0, 0x7), (7.0, 0x7), (1e9, 0x7), (-0.25, 0x8), (-0.0, 0x8),
+             (0.0, 0x0), (-6.0, 0xF), (-100.0, 0xF), (0.2500001, 0x1), (0.7499999, 0x1)]
+    for q, code in cases:
+        assert oracle.e2m1_encode(q) == code, (q, oracle.e2m1_encode(q), code)
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 2 ** 32, 500_000, dtype=np.uint64).astype(np.uint32)
+    bits = np.concatenate([bits, np.array([0x3F808000, 0x3F818000, 0x7F7FFFFF, 0x00008000,
+                                           0x80018000, 0x3F80FFFF], dtype=np.uint32)])
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ours = np.array([oracle.f32_to_bf16(v) for v in x[:60_000]], dtype=np.uint16)
+    assert np.array_equal(ours, ref[:60_000])
+
+
+# ----------------------------------------------------------------- SwiGLU ---
+
+def test_silu_table_is_correctly_rounded_mpmath():
+    """Every finite BF16 gate: the table entry is the BF16 value nearest to
+    silu(g) evaluated with 200-bit mpmath (never a near tie in that
+    precision, because silu(g) is irrational for g != 0)."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.prec = 200
+    tab, unresolved = oracle.silu_table()
+    assert unresolved == 0
+    g_all = synth.bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    t_all = synth.bf16_to_f32(tab)
+    below = synth.bf16_to_f32(((tab.astype(np.int32) - 1) & 0xFFFF).astype(np.uint16))
+    above = synth.bf16_to_f32(((tab.astype(np.int32) + 1) & 0xFFFF).astype(np.uint16))
+    checked = 0
+    for i in range(65536):
+        g = float(g_all[i])
+        if not math.isfinite(g):
+            continue
+        x = mpmath.mpf(g)
+        v = x / (1 + mpmath.exp(-x))
+        t = mpmath.mpf(float(t_all[i]))
+        if v == 0:
+            assert t == 0
+            continue
+        # the chosen value is at least as close as both neighbours
+        for nb in (below[i], above[i]):
+            if math.isfinite(float(nb)):
+                assert abs(v - t) <= abs(v - mpmath.mpf(float(nb))), (hex(i), g)
+        checked += 1
+    assert checked > 60000
+
+
+def test_silu_invariants():
+    tab, _ = oracle.silu_table()
+    assert tab[0x0000] == 0x0000 and tab[0x8000] == 0x8000
+    assert tab[0x7F80] == 0x7F80                     # silu(+inf) = +inf
+    g = synth.bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    s = synth.bf16_to_f32(tab)
+    fin = np.isfinite(g)
+    assert np.all(np.isnan(s[~fin & ~((g == np.inf))]))  # -inf and NaN gates -> NaN
+    big = fin & (g >= 8.0)
+    assert np.array_equal(s[big], g[big])            # silu(g) rounds to g for g >= 8
+    neg = fin & (g < 0)
+    assert np.all(s[neg] <= 0) and np.all(np.signbit(s[neg]))
+    tiny = fin & (np.abs(g) < 2.0 ** -20) & (np.abs(g) >= 2.0 ** -125)
+    assert np.array_equal(s[tiny], (g[tiny] / 2).astype(np.float32))
+    # g/2 below the BF16 normal range: when g/2 falls between two BF16 values
+    # the exact silu(g) = g/2 + g^2/4 - ... lies above the midpoint, so the
+    # result is the neighbour toward +inf
+    sub = fin & (np.abs(g) < 2.0 ** -125) & (g != 0)
+    half = (g[sub].astype(np.float64) / 2)
+    assert np.all(s[sub] >= half) and np.all(s[sub] - half <= 2.0 ** -134)
+    # monotone on g >= -1.278 (silu's minimum) and its known value at 1
+    assert tab[0x3F80] == 0x3F3B
+
+
+def test_swiglu_product_single_rounding_matches_torch():
+    """h = bf16(silu_bf16(g) * u): the product of two BF16 values is exact in
+    binary32, so torch's BF16 multiply of the same operands must agree."""
+    rng = np.random.default_rng(4)
+    gb = rng.integers(0, 65536, 20000).astype(np.uint16)
+    ub = rng.integers(0, 65536, 20000).astype(np.uint16)
+    tab, _ = oracle.silu_table()
+    ours = np.array([oracle.swiglu_bf16(int(a), int(b)) for a, b in zip(gb, ub)], dtype=np.uint16)
+    sig = torch.from_numpy(tab[gb].view(np.int16).copy()).view(torch.bfloat16)
+    up = torch.from_numpy(ub.view(np.int16).copy()).view(torch.bfloat16)
+    ref = (sig * up).view(torch.int16).numpy().view(np.uint16)
+    fin = np.isfinite(synth.bf16_to_f32(ref))
+    assert np.array_equal(ours[fin], ref[fin])
+
+
+# ------------------------------------------------------------ scale layout ---
+
+@pytest.mark.parametrize("rows,cols", [(37, 5376), (128, 7168), (200, 14336), (1, 48), (300, 272)])
+def test_scale_layout_is_a_bijection(rows, cols):
+    """Feature widths 5376, 7168 (the width that broke a width-specific
+    swizzle) and 14336: the tiled offset maps the padded [rows_pad, cpad]
+    scale grid one-to-one onto [0, scale_bytes)."""
+    rp = oracle.padded_rows(rows)
+    cp = oracle.scale_cols_padded(cols)
+    seen = np.zeros(oracle.scale_bytes(rows, cols), dtype=np.int32)
+    for r in range(rp):
+        for c in range(cp):
+            seen[oracle.scale_offset(r, c, cols)] += 1
+    assert np.all(seen == 1)
+
+
+def test_scale_layout_tile_structure():
+    """A 128 x 4 tile is one contiguous 512-byte chunk; the four columns of
+    one row are adjacent bytes; rows r and r+32 are 4 bytes apart, rows r and
+    r+1 16 bytes apart; tiles advance along columns before rows."""
+    cols = 7168
+    cp = oracle.scale_cols_padded(cols)
+    assert cp == 448
+    base = oracle.scale_offset(0, 0, cols)
+    tile = {oracle.scale_offset(r, c, cols) for r in range(128) for c in range(4)}
+    assert tile == set(range(base, base + 512))
+    assert oracle.scale_offset(5, 3, cols) - oracle.scale_offset(5, 2, cols) == 1
+    assert oracle.scale_offset(37, 1, cols) - oracle.scale_offset(5, 1, cols) == 4
+    assert oracle.scale_offset(6, 1, cols) - oracle.scale_offset(5, 1, cols) == 16
+    assert oracle.scale_offset(0, 4, cols) == 512
+    assert oracle.scale_offset(128, 0, cols) == (cp // 4) * 512
+
+
+# ------------------------------------------------------------- footprint ---
+
+def test_footprint_matches_pages(golden_dir):
+    fp = json.load(open(os.path.join(golden_dir, "footprint.json")))
+    m, md, n, k = fp["logical_m"], fp["descriptor_m"], fp["n"], fp["k"]
+    per_row = k // 2 + k // 16
+    assert md * per_row == fp["activation_qdata_plus_scales"]
+    assert oracle.qdata_bytes(n, k) + oracle.scale_bytes(n, k) == fp["weight_qdata_plus_scales"]
+    assert md * n * 2 == fp["padded_bf16_output"]
+    assert (fp["activation_qdata_plus_scales"] + fp["weight_qdata_plus_scales"]
+            + fp["padded_bf16_output"]) == fp["one_pass_total"]
+    mt = oracle.padded_rows(m) // 128
+    nt = n // 128
+    assert [mt, nt] == fp["grid"] and mt * nt == fp["ctas"] and mt == fp["weight_reuse"]
+    assert mt * fp["weight_qdata_plus_scales"] == fp["requested_weight_bytes"]
+    a_bytes = oracle.qdata_bytes(m, k) + oracle.scale_bytes(m, k)
+    assert nt * a_bytes == fp["requested_activation_bytes"]
+    # The page prints a total 3,072 B above the sum of its two printed parts;
+    # both parts are reproduced exactly above, the printed total is not.
+    assert fp["requested_total"] - (fp["requested_weight_bytes"]
+                                    + fp["requested_activation_bytes"]) == 3072
+
+
+# --------------------------------------------------------- quantisation ---
+
+def _bf16_bits(vals):
+    t = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)
+    assert torch.equal(t.to(torch.float32), torch.tensor(vals, dtype=torch.float32))
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_hand_worked_blocks(golden_dir):
+    fx = json.load(open(os.path.join(golden_dir, "hand_blocks.json")))
+    cols = fx["cols"]
+    row = fx["rows"][0]
+    x = _bf16_bits(row["values"]).reshape(1, cols)
+    q, s, rec = oracle.quantize(x, cols, swiglu=False)
+    assert rec["status"] == 0
+    assert float(np.uint32(rec["amax_bits"]).view(np.float32)) == row["amax"]
+    assert rec["global_scale"] == np.float32(row["global_scale"])
+    assert list(q[0]) == row["qdata"]
+    assert [int(s[oracle.scale_offset(0, c, cols)]) for c in range(3)] == row["scale_codes"]
+    assert s[oracle.scale_offset(0, 3, cols)] == 0              # pad scale column
+    assert not q[1:].any() and int(s.sum()) == sum(row["scale_codes"])  # pad rows zero
+
+
+def test_global_scale_is_amax_over_2688():
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        amax = np.float32(rng.uniform(0.01, 1000.0))
+        x = np.zeros((3, 32), dtype=np.float32)
+        x[1, 7] = -amax
+        xb = torch.from_numpy(x).to(torch.bfloat16)
+        a = float(xb.abs().max())
+        _, _, rec = oracle.quantize(xb.view(torch.int16).numpy().view(np.uint16), 32, False)
+        assert rec["global_scale"] == np.float32(np.float32(a) / np.float32(2688.0))
+
+
+def test_zero_tensor_and_nonfinite():
+    x = np.zeros((5, 64), dtype=np.uint16)
+    q, s, rec = oracle.quantize(x, 64, False)
+    assert rec["status"] == 0 and rec["global_scale"] == 0 and not q.any() and not s.any()
+    x[2, 3] = 0x7F80  # +inf
+    q, s, rec = oracle.quantize(x, 64, False)
+    assert rec["status"] == oracle.ENONFINITE and np.isnan(rec["global_scale"])
+    assert not q.any() and not s.any()
+    x = np.zeros((2, 2 * 32), dtype=np.uint16)
+    x[1, 5] = 0xFF80  # gate = -inf -> silu NaN -> h NaN
+    _, _, rec = oracle.quantize(x, 32, True)
+    assert rec["status"] == oracle.ENONFINITE
+
+
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_round_trip_bounds(swiglu):
+    """|h - deq(h)| <= s * (half the E2M1 gap at h/s) for |h/s| <= 6;
+    dequantised block max within 2^-4 (E4M3 rounding) of the block max for
+    normal-range scales; scale codes <= 0x7E; pad region zero."""
+    m, k = 70, 256
+    x = synth.activation(m, k, seed=11) if swiglu else synth.quant_input(m, k, seed=11)
+    q, s, rec = oracle.quantize(x, k, swiglu)
+    g = float(rec["global_scale"])
+    if swiglu:
+        tab, _ = oracle.silu_table()
+        gt = synth.bf16_to_f32(tab[x[:, :k]]).astype(np.float32)
+        h = torch.from_numpy(gt * synth.bf16_to_f32(x[:, k:])).to(torch.bfloat16).float().numpy()
+    else:
+        h = synth.bf16_to_f32(x)
+    deq = oracle.dequantize_rows(q, s, g, k, np.arange(m))
+    assert s.max() <= 0x7E
+    mags = np.array([oracle.e2m1_value(c) for c in range(8)])
+    for r in range(m):
+        for b in range(k // 16):
+            sc = np.float32(oracle.e4m3_value(int(s[oracle.scale_offset(r, b, k)])) * np.float32(g))
+            blk = h[r, b * 16:(b + 1) * 16].astype(np.float64)
+            d = deq[r, b * 16:(b + 1) * 16]
+            if sc == 0:
+                assert not d.any()
+                continue
+            t = np.abs(blk / float(sc))
+            idx = np.clip(np.searchsorted(mags, t), 1, 7)
+            gap = mags[idx] - mags[idx - 1]
+            assert np.all(np.abs(blk - d) <= float(sc) * gap / 2 * (1 + 1e-6) + 1e-30)
+            bmax = np.abs(blk).max()
+            ratio = bmax / (6 * g)
+            if 2.0 ** -6 <= ratio <= 448:
+                assert abs(float(sc) * 6 - bmax) <= bmax * 2.0 ** -4 * 1.001
+    assert not q[m:].any()
+
+
+def test_oracle_gemm_matches_numpy_fp64_matmul():
+    """Tiny shapes: the oracle GEMM equals an independent FP64 matmul of the
+    dequantised operands (same values; only the summation order differs),
+    and the unquantised matmul agrees to NVFP4 accuracy."""
+    m, n, k = 37, 48, 256
+    x = synth.activation(m, k, seed=3)
+    w = synth.weight(n, k, seed=3)
+    aq, as_, ar = oracle.quantize(x, k, True)
+    wq, ws, wr = oracle.quantize(w, k, False)
+    ref = oracle.gemm_rows(aq, as_, ar["global_scale"], wq, ws, wr["global_scale"], n, k, np.arange(m))
+    A = oracle.dequantize_rows(aq, as_, ar["global_scale"], k, np.arange(m))
+    W = oracle.dequantize_rows(wq, ws, wr["global_scale"], k, np.arange(n))
+    mm = A @ W.T
+    terms = np.abs(A) @ np.abs(W).T
+    assert np.all(np.abs(ref - mm) <= 1e-12 * terms + 1e-300)
+    # transposed-operand guard: a wrong operand order gives a different shape or values
+    assert ref.shape == (m, n)
+    tab, _ = oracle.silu_table()
+    h = torch.from_numpy(synth.bf16_to_f32(tab[x[:, :k]]) * synth.bf16_to_f32(x[:, k:])).to(
+        torch.bfloat16).double().numpy()
+    exact = h @ synth.bf16_to_f32(w).astype(np.float64).T
+    rel = np.linalg.norm(ref - exact) / np.linalg.norm(exact)
+    assert rel < 0.2
+
+
+def test_gemm_tolerance_helper():
+    ref = np.array([1.0, -2.0, 0.0, 100.0])
+    ok, worst = oracle.check_gemm_tolerance(ref * (1 + 0.009), ref)
+    assert ok
+    ok, _ = oracle.check_gemm_tolerance(ref * 1.05, ref)
+    assert not ok
