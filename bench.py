@@ -1,0 +1,351 @@
+"""Benchmark of the NVFP4 FC2 step on GB300.
+
+One step = the whole hot path on the canonical FC2 workload (M=37,810,
+N=5,376, K=14,336): weight quantise (BF16 [N,K] -> NVFP4), SwiGLU producer
+(gate|up BF16 [M,2K] -> NVFP4 [37,888, K]) and the block-scaled GEMM (BF16
+[M,N] out).  Inputs are seeded synthetic tensors of the pages' shapes and
+value laws, resident in HBM before the timed region; the 2.17 GB gate|up
+input is larger than L2, so no flush is needed between steps.
+
+Metric: dense FC2 throughput, 2*M*N*K / step time, in TFLOP/s (the GEMM's
+TFLOP/s and the producer's milliseconds are reported beside it).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+replica of the step (the path does not shard), timing is the max over ranks
+and `value` sums the ranks' work.  `--impl reference` times the CPU oracle
+on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K = 37810, 5376, 14336
+FLOP = 2 * M * N * K
+METRIC = "FC2 NVFP4 step TFLOP/s (2MNK / (weight quant + SwiGLU producer + GEMM)); GEMM TFLOP/s and producer ms reported"
+WORKLOAD = "canonical FC2: gate|up bf16 [37810, 2x14336] N(0,1)+0.1% x20 -> SwiGLU -> NVFP4; W bf16 [5376,14336] N(0,1/sqrt(K)) -> NVFP4; block-scaled GEMM FP32 acc -> bf16 [37810,5376]; seed 0"
+# The pages' producer + FC2 p50 on GB10 for this workload ("FC2 NVFP4
+# Scheduling Results", Timing): 38.823 ms -> 2MNK / 38.823 ms.
+PAGES_STEP_MS = 38.823
+PAGES_TFLOPS = FLOP / (PAGES_STEP_MS * 1e-3) / 1e12
+
+
+def producer_bytes(m, k):
+    """Algorithmic bytes of the two-pass SwiGLU producer: gate|up read twice
+    plus QDATA and scales written once."""
+    import diffusion_transformer_mlp_gb300 as fc2
+    return 2 * (m * 2 * k * 2) + fc2.qdata_bytes(m, k) + fc2.scale_bytes(m, k)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.uuid = uuid
+        self.out = os.path.join("/tmp", f"fc2_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.out)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def cpu_baseline(seconds_target: float = 15.0):
+    """The oracle, as it stands, on the host cores: SwiGLU + two-pass
+    quantisation of a row sample of the canonical input, then the FP64 GEMM
+    of a smaller row sample against the full NVFP4 weight; scaled to the
+    metric's unit as 2*rows*N*K / time."""
+    import numpy as np
+
+    import oracle
+    import synth
+    rows_q, rows_g = 512, 8
+    x = synth.activation(rows_q, K, seed=0)
+    w = synth.weight(N, K, seed=0)
+    wq, ws, wr = oracle.quantize(w, K, swiglu=False)
+    t0 = time.perf_counter()
+    aq, as_, ar = oracle.quantize(x, K, swiglu=True)
+    t_q = (time.perf_counter() - t0) / rows_q
+    t0 = time.perf_counter()
+    oracle.gemm_rows(aq, as_, ar["global_scale"], wq, ws, wr["global_scale"], N, K, np.arange(rows_g))
+    t_g = (time.perf_counter() - t0) / rows_g
+    per_row = t_q + t_g
+    tflops = 2 * N * K / per_row / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"SwiGLU+two-pass quantise of {rows_q} rows x K={K} ({t_q * 1e3:.3f} ms/row) and FP64 "
+                      f"dequantise-GEMM of {rows_g} rows x N={N} (incl. weight dequantisation, "
+                      f"{t_g * 1e3:.1f} ms/row); rows/s = {1.0 / per_row:.2f}",
+            "rows_per_s": 1.0 / per_row}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    base = cpu_baseline()
+    per_row_s = 1.0 / base["rows_per_s"]
+    step_s = per_row_s * M
+    line = {"metric": METRIC, "value": base["value"], "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64-oracle", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
+                       "note": "each step is a bounded row sample of the workload, extrapolated to all M rows"},
+            "impl": "reference", "cpu_baseline": {k: base[k] for k in ("kind", "cores", "sample")} | {
+                "value": base["value"], "unit": "TFLOP/s"},
+            "e2e": {"value": base["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def traffic_record(kernel: str):
+    """ncu DRAM bytes per launch for `kernel`, if profiles/traffic.json holds a
+    capture taken on the current source of that kernel."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "diffusion_transformer_mlp_gb300", "csrc", rec["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import diffusion_transformer_mlp_gb300 as fc2
+    import synth
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    fc2.load()
+    peaks = load_peaks()
+
+    # ---- inputs (host synth -> HBM) and buffers
+    x_host = torch.empty(M, 2 * K, dtype=torch.bfloat16).pin_memory()
+    synth.activation(M, K, seed=0, out=x_host.view(torch.int16).numpy().view(np.uint16))
+    w_host = synth.weight(N, K, seed=0)
+    x = x_host.to(dev)
+    w = torch.from_numpy(w_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    wq = fc2.empty_nvfp4(N, K, dev)
+    act = fc2.empty_nvfp4(M, K, dev)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fc2.nvfp4_quantize_weight(w, wq, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fc2.swiglu_nvfp4_quantize(x, act, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fc2.nvfp4_fc2_gemm(act, wq, out, status, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0 or fc2.read_rec(act)["status"] != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region: K steps, events around each kernel group
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    wq_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    prod_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    gemm_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if int(status.item()) != 0:
+        raise RuntimeError("GEMM reported a device timeout")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * FLOP / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public host-buffer call
+    e2e_steps = max(3, min(args.steps, 20))
+    ws = {}
+    out_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        fc2.nvfp4_quantize_weight(w, wq, stream)
+        fc2.fc2_host(x_host, wq, ws, stream, out_host)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        fc2.nvfp4_quantize_weight(w, wq, stream)
+        fc2.fc2_host(x_host, wq, ws, stream, out_host)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * FLOP / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+           "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2,
+           "steps": e2e_steps, "api": "nvfp4_quantize_weight + fc2_host (pinned host gate|up in, host BF16 out)"}
+
+    # ---- roofline of the dominant kernel
+    gemm_tflops = FLOP / (gemm_ms * 1e-3) / 1e12
+    fp4_peak = peaks["bf16_tflops"] * 6.0  # dense FP4 / BF16 nominal ratio 13.5 / 2.25
+    pbytes = producer_bytes(M, K)
+    prod_gbs = pbytes / (prod_ms * 1e-3) / 1e9
+    kernels = {
+        "gemm": {"ms": gemm_ms, "tflops": gemm_tflops, "frac_of_fp4_peak": gemm_tflops / fp4_peak},
+        "swiglu_producer": {"ms": prod_ms, "algorithmic_bytes": pbytes, "gbs": prod_gbs,
+                            "frac_of_hbm": prod_gbs / peaks["hbm_gbs"],
+                            "one_read_bytes": M * 2 * K * 2 + fc2.qdata_bytes(M, K) + fc2.scale_bytes(M, K)},
+        "weight_quant": {"ms": wq_ms},
+    }
+    if gemm_ms >= prod_ms:
+        roofline = {"kernel": "k_fc2_gemm", "bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak,
+                    "unit": "TFLOP/s", "frac": gemm_tflops / fp4_peak, "traffic": traffic_record("k_fc2_gemm"),
+                    "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"}
+    else:
+        roofline = {"kernel": "k_quant+k_amax (SwiGLU producer)", "bound": "hbm", "achieved": prod_gbs,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": prod_gbs / peaks["hbm_gbs"],
+                    "traffic": traffic_record("swiglu_producer"),
+                    "peak_source": f"{peaks['source']} HBM copy"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": value / PAGES_TFLOPS, "dtype": "nvfp4 (e2m1 x ue4m3, fp32 acc, bf16 out)",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 (gate|up 2.17 GB per step), no flush"},
+                "gemm_tflops": gemm_tflops, "producer_ms": prod_ms, "weight_quant_ms": wq_ms, "gemm_ms": gemm_ms,
+                "kernels": kernels, "roofline": roofline, "clocks": clocks, "e2e": e2e,
+                "gpu_launches": 5 * args.steps,
+                "baseline_context": {"pages_gb10_producer_plus_fc2_ms": PAGES_STEP_MS,
+                                     "pages_gb10_tflops": PAGES_TFLOPS}}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"].pop("rows_per_s", None)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

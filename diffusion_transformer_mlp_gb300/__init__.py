@@ -1,0 +1,180 @@
+"""NVFP4 FC2 step of a video diffusion transformer MLP on GB300 (sm_103a).
+
+Python face of libnvfp4fc2.so.  Each function forwards to the C entry point
+of the same name; PyTorch provides device memory and the current stream.
+
+    w_q  = nvfp4_quantize_weight(w_bf16)                 # once per weight
+    a_q  = swiglu_nvfp4_quantize(gate_up_bf16)           # per step
+    out  = nvfp4_fc2_gemm(a_q, w_q)                      # per step
+    out  = fc2(gate_up_bf16, w_q)                        # both per-step calls
+    out  = fc2_host(gate_up_host, w_q)                   # host in, host out
+
+Sources: "FC2 NVFP4 Scheduling Results" (Canonical Operation; Production
+Integration: forward_swiglu = accepted producer, then the FC2 GEMM) and
+"GB10 component-2 nsys summary" (nvfp4; native_pack_validation).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import NVFP4Error, load  # noqa: F401
+
+__all__ = ["NVFP4Tensor", "NVFP4Error", "load", "padded_rows", "qdata_bytes", "scale_bytes", "scale_offset",
+           "nvfp4_quantize_weight", "swiglu_nvfp4_quantize", "nvfp4_fc2_gemm", "fc2", "fc2_host",
+           "empty_nvfp4", "read_rec"]
+
+
+def padded_rows(rows: int) -> int:
+    return int(load().nvfp4_padded_rows(rows))
+
+
+def qdata_bytes(rows: int, cols: int) -> int:
+    return int(load().nvfp4_qdata_bytes(rows, cols))
+
+
+def scale_bytes(rows: int, cols: int) -> int:
+    return int(load().nvfp4_scale_bytes(rows, cols))
+
+
+def scale_offset(r: int, c: int, cols: int) -> int:
+    return int(load().nvfp4_scale_offset(r, c, cols))
+
+
+@dataclass
+class NVFP4Tensor:
+    """Device NVFP4 tensor: QDATA [padded_rows, cols/2] uint8, tiled scales,
+    and the 16-byte global-scale record (float32 g, u32 amax bits, u32
+    status, reserved), all on one CUDA device."""
+    qdata: torch.Tensor
+    scales: torch.Tensor
+    rec: torch.Tensor
+    rows: int
+    cols: int
+
+    @property
+    def device(self) -> torch.device:
+        return self.qdata.device
+
+
+def empty_nvfp4(rows: int, cols: int, device="cuda") -> NVFP4Tensor:
+    q = torch.empty(qdata_bytes(rows, cols), dtype=torch.uint8, device=device).view(padded_rows(rows), cols // 2)
+    s = torch.empty(scale_bytes(rows, cols), dtype=torch.uint8, device=device)
+    rec = torch.empty(16, dtype=torch.uint8, device=device)
+    return NVFP4Tensor(q, s, rec, rows, cols)
+
+
+def read_rec(t: NVFP4Tensor) -> dict:
+    """Copy the record to the host (synchronises)."""
+    r = t.rec.cpu()
+    return {"global_scale": float(r[0:4].view(torch.float32)[0]),
+            "amax_bits": int(r[4:8].view(torch.int32)[0]) & 0xFFFFFFFF,
+            "status": int(r[8:12].view(torch.int32)[0])}
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_dev(*ts: torch.Tensor) -> torch.device:
+    dev = ts[0].device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for t in ts:
+        if t.device != dev:
+            raise ValueError("tensors must be on one CUDA device")
+    return dev
+
+
+def _bf16_matrix(x: torch.Tensor, name: str) -> torch.Tensor:
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D bfloat16 tensor")
+    if x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its rows")
+    return x
+
+
+def nvfp4_quantize_weight(w: torch.Tensor, out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
+    _bf16_matrix(w, "w")
+    rows, cols = w.shape
+    out = out or empty_nvfp4(rows, cols, w.device)
+    dev = _check_dev(w, out.qdata, out.scales, out.rec)
+    with torch.cuda.device(dev):
+        _lib.check(load().nvfp4_quantize_weight(_ptr(w), rows, cols, w.stride(0), _ptr(out.qdata), _ptr(out.scales),
+                                                _ptr(out.rec), _stream(stream)), "nvfp4_quantize_weight")
+    return out
+
+
+def swiglu_nvfp4_quantize(gate_up: torch.Tensor, out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
+    _bf16_matrix(gate_up, "gate_up")
+    m, two_k = gate_up.shape
+    if two_k % 2:
+        raise ValueError("gate_up must have an even number of columns (gate | up)")
+    k = two_k // 2
+    out = out or empty_nvfp4(m, k, gate_up.device)
+    dev = _check_dev(gate_up, out.qdata, out.scales, out.rec)
+    with torch.cuda.device(dev):
+        _lib.check(load().swiglu_nvfp4_quantize(_ptr(gate_up), m, k, gate_up.stride(0), _ptr(out.qdata),
+                                                _ptr(out.scales), _ptr(out.rec), _stream(stream)),
+                   "swiglu_nvfp4_quantize")
+    return out
+
+
+def nvfp4_fc2_gemm(a: NVFP4Tensor, w: NVFP4Tensor, out: torch.Tensor | None = None,
+                   status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if a.cols != w.cols:
+        raise ValueError("activation and weight K differ")
+    m, n, k = a.rows, w.rows, a.cols
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=a.device)
+    if out.dtype != torch.bfloat16 or out.dim() != 2 or out.shape[0] < m or out.shape[1] < n or out.stride(1) != 1:
+        raise ValueError("out must be a bfloat16 [>=m, >=n] tensor with unit column stride")
+    dev = _check_dev(a.qdata, a.scales, a.rec, w.qdata, w.scales, w.rec, out)
+    st_ptr = ctypes.c_void_p(status.data_ptr()) if status is not None else ctypes.c_void_p(0)
+    with torch.cuda.device(dev):
+        _lib.check(load().nvfp4_fc2_gemm(_ptr(a.qdata), _ptr(a.scales), _ptr(a.rec), _ptr(w.qdata), _ptr(w.scales),
+                                         _ptr(w.rec), m, n, k, _ptr(out), out.stride(0), st_ptr, _stream(stream)),
+                   "nvfp4_fc2_gemm")
+    return out
+
+
+def fc2(gate_up: torch.Tensor, w: NVFP4Tensor, act: NVFP4Tensor | None = None, out: torch.Tensor | None = None,
+        stream=None) -> torch.Tensor:
+    """One FC2 step on device tensors: SwiGLU + NVFP4 quantise, then GEMM."""
+    act = swiglu_nvfp4_quantize(gate_up, act, stream)
+    return nvfp4_fc2_gemm(act, w, out, None, stream)
+
+
+def fc2_host(gate_up_host: torch.Tensor, w: NVFP4Tensor, workspace: dict | None = None, stream=None,
+             out_host: torch.Tensor | None = None) -> torch.Tensor:
+    """FC2 from host memory to host memory: copy gate|up to the device, run
+    the step, copy the BF16 output back.  Pinned host tensors make the copies
+    asynchronous; `workspace` (a dict) keeps device buffers between calls."""
+    m, two_k = gate_up_host.shape
+    k = two_k // 2
+    ws = workspace if workspace is not None else {}
+    dev = w.device
+    key = (m, k, w.rows)
+    if ws.get("key") != key:
+        ws.clear()
+        ws["key"] = key
+        ws["x"] = torch.empty(m, two_k, dtype=torch.bfloat16, device=dev)
+        ws["act"] = empty_nvfp4(m, k, dev)
+        ws["out"] = torch.empty(m, w.rows, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    with torch.cuda.stream(s):
+        ws["x"].copy_(gate_up_host, non_blocking=True)
+        fc2(ws["x"], w, ws["act"], ws["out"], s)
+        if out_host is None:
+            out_host = torch.empty(m, w.rows, dtype=torch.bfloat16, pin_memory=True)
+        out_host.copy_(ws["out"], non_blocking=True)
+    s.synchronize()
+    return out_host

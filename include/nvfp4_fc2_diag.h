@@ -1,0 +1,53 @@
+/*
+ * nvfp4_fc2_diag.h -- diagnostic entry points of libnvfp4fc2.so.
+ *
+ * They run the exact device functions the production kernels use (the BF16
+ * silu, the E2M1 and E4M3 encoders, the bounded pipeline wait) on inputs the
+ * tests choose, so that each can be checked exhaustively against the CPU
+ * oracle.  They are not on the FC2 path.  Same conventions as nvfp4_fc2.h:
+ * device pointers, caller-owned memory, asynchronous on `stream`, synchronous
+ * argument errors.
+ */
+#ifndef NVFP4_FC2_DIAG_H
+#define NVFP4_FC2_DIAG_H
+
+#include <stdint.h>
+#include "nvfp4_fc2.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* out[g] = BF16 bits of the producer's silu for every BF16 gate g
+ * (65536 entries, device).  The SwiGLU step of the activation producer:
+ * "GB10 component-2 nsys summary", other_boundaries (separate BF16 silu). */
+nvfp4_status nvfp4_diag_silu_all(uint16_t* out, nvfp4_stream_t stream);
+
+/* h[i] = the producer's SwiGLU output for (gate[i], up[i]), BF16 bits,
+ * n elements (device arrays). */
+nvfp4_status nvfp4_diag_swiglu(const uint16_t* gate, const uint16_t* up, uint16_t* h, int64_t n,
+                               nvfp4_stream_t stream);
+
+/* Scan every binary32 bit pattern p in [0, 2^32) through the device encoder
+ * (which = 0: E2M1 element code, which = 1: E4M3 block-scale code) and list
+ * the patterns where the code differs from that of p - 1, skipping pairs
+ * where either pattern is Inf or NaN.  Entry i of `trans` is
+ * {p, code(p), code(p-1)}; code of pattern 0 goes to first_code.  At most
+ * `cap` entries are stored; *count (device) receives the number found.
+ * All of trans, count, first_code are device memory; *count must be zero on
+ * entry. */
+nvfp4_status nvfp4_diag_code_transitions(int which, uint32_t* trans, uint32_t cap,
+                                         uint32_t* count, uint32_t* first_code,
+                                         nvfp4_stream_t stream);
+
+/* Run the bounded wait used by the GEMM pipeline on an mbarrier that nothing
+ * arrives at, with the given limit in nanoseconds (1 .. 10^9).  Writes
+ * NVFP4_ETIMEOUT to *dev_status when the wait runs out (device uint32).
+ * Exercises the timeout path without faulting or hanging the GPU. */
+nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status,
+                                     nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_FC2_DIAG_H */

@@ -1,0 +1,112 @@
+"""Exhaustive device checks of the producer's building blocks against the
+oracle: the BF16 silu over all 65,536 gates, the SwiGLU product, and the
+E2M1 / E4M3 encoders over every finite binary32 bit pattern."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from diffusion_transformer_mlp_gb300 import _lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _stream():
+    import ctypes
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _p(t):
+    import ctypes
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def test_device_silu_all_65536_gates_equal_oracle():
+    out = torch.empty(65536, dtype=torch.int16, device="cuda")
+    _lib.check(_lib.load().nvfp4_diag_silu_all(_p(out), _stream()), "silu")
+    dev = out.cpu().numpy().view(np.uint16)
+    ref, unresolved = oracle.silu_table()
+    assert unresolved == 0
+    gf = synth.bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    rf = synth.bf16_to_f32(ref)
+    both_nan = np.isnan(synth.bf16_to_f32(dev)) & np.isnan(rf)
+    bad = np.nonzero((dev != ref) & ~both_nan)[0]
+    assert bad.size == 0, [(hex(i), float(gf[i]), hex(dev[i]), hex(ref[i])) for i in bad[:10]]
+
+
+def test_device_swiglu_equals_oracle():
+    rng = np.random.default_rng(7)
+    n = 1 << 18
+    g = rng.integers(0, 65536, n).astype(np.uint16)
+    u = rng.integers(0, 65536, n).astype(np.uint16)
+    # plus the N(0,1) region densely
+    g[: n // 2] = synth.normal_bf16((n // 2,), 5, 0, 1.0, 1e-3)
+    u[: n // 2] = synth.normal_bf16((n // 2,), 5, 1, 1.0, 1e-3)
+    tg = torch.from_numpy(g.view(np.int16)).cuda()
+    tu = torch.from_numpy(u.view(np.int16)).cuda()
+    th = torch.empty_like(tg)
+    _lib.check(_lib.load().nvfp4_diag_swiglu(_p(tg), _p(tu), _p(th), n, _stream()), "swiglu")
+    dev = th.cpu().numpy().view(np.uint16)
+    tab, _ = oracle.silu_table()
+    ref = np.array([oracle.swiglu_bf16(int(a), int(b)) for a, b in zip(g[:20000], u[:20000])], dtype=np.uint16)
+    fin = ~np.isnan(synth.bf16_to_f32(ref))
+    assert np.array_equal(dev[:20000][fin], ref[fin])
+    assert np.all(np.isnan(synth.bf16_to_f32(dev[:20000][~fin])))
+
+
+def _oracle_transitions(which: int):
+    """Transitions of the oracle encoder over the ordered bit patterns, found
+    by bisection (the encoders are monotone in |x| within each sign)."""
+    enc = oracle.e2m1_encode if which == 0 else oracle.e4m3_encode
+
+    def code(bits):
+        return enc(float(np.uint32(bits).view(np.float32)))
+
+    out = []
+    for lo, hi in ((0x00000000, 0x7F7FFFFF), (0x80000000, 0xFF7FFFFF)):
+        p = lo + 1
+        cur = code(lo)
+        while p <= hi:
+            # first pattern in [p, hi] whose code differs from cur
+            if code(hi) == cur:
+                break
+            a, b = p, hi
+            while a < b:
+                mid = (a + b) // 2
+                if code(mid) != cur:
+                    b = mid
+                else:
+                    a = mid + 1
+            new = code(a)
+            out.append((a, new, cur))
+            cur = new
+            p = a + 1
+    return sorted(out)
+
+
+@pytest.mark.parametrize("which", [0, 1], ids=["e2m1", "e4m3"])
+def test_device_encoder_transitions_equal_oracle(which):
+    cap = 4096
+    trans = torch.zeros(3 * cap, dtype=torch.int32, device="cuda")
+    count = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _lib.check(_lib.load().nvfp4_diag_code_transitions(which, _p(trans), cap, _p(count), _p(first), _stream()),
+               "transitions")
+    n = int(count.item())
+    assert 0 < n <= cap
+    t = trans[: 3 * n].cpu().numpy().view(np.uint32).reshape(n, 3)
+    dev = sorted(tuple(int(v) for v in row) for row in t)
+    ref = _oracle_transitions(which)
+    assert int(first.item()) == (oracle.e2m1_encode(0.0) if which == 0 else oracle.e4m3_encode(0.0))
+    assert dev == ref, (len(dev), len(ref), [x for x in dev if x not in ref][:5], [x for x in ref if x not in dev][:5])
+
+
+def test_bounded_wait_reports_timeout_without_hanging():
+    st = torch.full((1,), 77, dtype=torch.int32, device="cuda")
+    _lib.check(_lib.load().nvfp4_diag_wait_timeout(2_000_000, _p(st), _stream()), "wait")
+    torch.cuda.synchronize()
+    assert int(st.item()) == _lib.NVFP4_ETIMEOUT
+    # the context is still usable
+    x = torch.ones(4, device="cuda")
+    assert float((x + 1).sum().item()) == 8.0

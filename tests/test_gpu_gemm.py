@@ -1,0 +1,125 @@
+"""GEMM parity on the GPU: BF16 output against the oracle's unrounded FP64
+reference, |gpu - ref| <= 1e-2|ref| + 1e-3 rms(ref) elementwise -- on all
+rows for the tiny and mid FC2 workloads and small shapes that span several
+tiles and a ragged M tail, on 1024 seeded rows (seed + 7) for the canonical
+and ragged-M workloads; plus row invariance across M, run-to-run
+determinism, untouched bytes outside [m, n], and the status word."""
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_mlp_gb300 as fc2
+import oracle
+import synth
+from _util import gemm_check, sample_rows, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def build_case(m, n, k, seed):
+    x = synth.activation(m, k, seed=seed)
+    w = synth.weight(n, k, seed=seed)
+    a_ref = oracle.quantize(x, k, swiglu=True)
+    w_ref = oracle.quantize(w, k, swiglu=False)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    w_dev = fc2.nvfp4_quantize_weight(wd)
+    a_dev = fc2.swiglu_nvfp4_quantize(xd)
+    return a_ref, w_ref, a_dev, w_dev, xd
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 512, 1024), (128, 128, 256), (200, 256, 512), (1, 128, 256),
+                                   (1000, 384, 2048), (333, 640, 768)])
+def test_gemm_all_rows_small(m, n, k):
+    a_ref, w_ref, a_dev, w_dev, _ = build_case(m, n, k, seed=m + n + k)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    (ok, worst), ref, got = gemm_check(out, a_ref, w_ref, np.arange(m), n, k)
+    assert ok, f"worst error / bound = {worst}"
+
+
+def test_gemm_mid_all_rows():
+    """Mid FC2: M=4096, K=14336, N=5376, full-output check."""
+    m, n, k = 4096, 5376, 14336
+    a_ref, w_ref, a_dev, w_dev, _ = build_case(m, n, k, seed=0)
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, np.arange(m), n, k)
+    assert ok, f"worst error / bound = {worst}"
+
+
+def test_gemm_output_bounds_untouched():
+    """Rows >= m and columns >= n of a wider output buffer keep their bytes."""
+    m, n, k = 130, 256, 512
+    _, _, a_dev, w_dev, _ = build_case(m, n, k, seed=4)
+    big = torch.full((m + 7, n + 40), 3.0, dtype=torch.bfloat16, device="cuda")
+    fc2.nvfp4_fc2_gemm(a_dev, w_dev, out=big[:, : n + 40])
+    torch.cuda.synchronize()
+    assert torch.all(big[m:] == 3.0) and torch.all(big[:m, n:] == 3.0)
+    assert not torch.all(big[:m, :n] == 3.0)
+
+
+def test_gemm_nonfinite_record_propagates_nan():
+    m, n, k = 64, 128, 256
+    _, _, a_dev, w_dev, xd = build_case(m, n, k, seed=5)
+    xd[3, 7] = float("inf")
+    a_dev = fc2.swiglu_nvfp4_quantize(xd)
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    assert fc2.read_rec(a_dev)["status"] == fc2._lib.NVFP4_ENONFINITE
+    assert torch.isnan(out.float()).all()
+
+
+@pytest.fixture(scope="module")
+def canonical():
+    m, n, k = 37810, 5376, 14336
+    return (m, n, k) + build_case(m, n, k, seed=0)
+
+
+def test_gemm_canonical_sampled_rows(canonical):
+    m, n, k, a_ref, w_ref, a_dev, w_dev, _ = canonical
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    rows = sample_rows(m, 1024, seed=0 + 7)
+    (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, rows, n, k)
+    assert ok, f"worst error / bound = {worst}"
+
+
+RAGGED = [37711, 37725, 37742, 37774, 37809, 37838, 37966, 38222]
+
+
+@pytest.mark.parametrize("m", RAGGED)
+def test_gemm_ragged_m(m):
+    """Ragged-M sweep: producer bytes exact, output rows within tolerance on
+    1024 sampled rows (always including the last row), 50 back-to-back runs
+    with identical bytes."""
+    n, k = 5376, 14336
+    from _util import compare_quant
+    a_ref, w_ref, a_dev, w_dev, xd = build_case(m, n, k, seed=0)
+    assert compare_quant(a_dev, *a_ref, m, k) is None
+    out0 = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    rows = sample_rows(m, 1024, seed=0 + 7)
+    (ok, worst), _, _ = gemm_check(out0, a_ref, w_ref, rows, n, k)
+    assert ok, f"M={m}: worst error / bound = {worst}"
+    out = torch.empty_like(out0)
+    for _ in range(50):
+        fc2.fc2(xd, w_dev, a_dev, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+
+
+def test_gemm_row_invariance_across_m(canonical):
+    """Output row r is bit-identical for every M of the ragged sweep (r < M):
+    the K reduction order does not depend on M.  The same NVFP4 activation
+    bytes are passed with each M (a row-major prefix of QDATA and whole
+    128-row scale panels)."""
+    m0, n, k, _, _, a_dev, w_dev, _ = canonical
+    base = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    for m in [37711, 37725, 37742, 37774, 37809, 1, 128, 129]:
+        a_m = fc2.NVFP4Tensor(a_dev.qdata, a_dev.scales, a_dev.rec, m, k)
+        out = fc2.nvfp4_fc2_gemm(a_m, w_dev)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), base[:m].view(torch.int16)), m
