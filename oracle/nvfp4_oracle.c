@@ -18,8 +18,8 @@
  *     (the general 128-row by 4-scale-column tiled scale offset).
  *   - "GB10 component-2 nsys summary", other_boundaries (unfused SwiGLU:
  *     a separate BF16 silu and a separate BF16 multiply).
- *   - The NVFP4 recipe of the benchmark spec: global = amax/(6*448),
- *     block = RNE-E4M3(block_amax/(6*global)),
+ *   - The two-level NVFP4 recipe (not printed on the pages):
+ *     global = amax/(6*448), block = RNE-E4M3(block_amax/(6*global)),
  *     element = RNE-E2M1(x/(block*global)).
  *
  * Readings where the pages are silent (each is listed in the design doc):
