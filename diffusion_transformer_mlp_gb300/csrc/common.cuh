@@ -184,6 +184,24 @@ __device__ __forceinline__ uint32_t e4m3_code(float r) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(v) : "f"(r));
   return v & 0xFFu;
 }
+// Two E2M1 codes in one byte: `lo` in bits 0..3, `hi` in bits 4..7 (the
+// first source operand of the packed conversion lands in the upper half).
+__device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+// Two binary32 values rounded to BF16 (nearest even) in one instruction;
+// `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Value of an unsigned E4M3 code 0x00..0x7E (exact in binary32).
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
   const uint32_t e = (c >> 3) & 15u, m = c & 7u;

@@ -31,80 +31,126 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSiluEntries = 3840;
+constexpr int kSegElems = 512;  // elements of one row handled by one warp per unit (16 per lane)
 
-// Correctly rounded BF16 silu for gates with exponent field 117..129 (g > 0)
-// and 117..133 (g < 0); generated at build time by gen_silu_table.py.
+// Correctly rounded BF16 silu for gates with exponent field 117..129 (g > 0,
+// entries 0..1663) and 117..133 (g < 0, entries 1664..3839), indexed by
+// (g & 0x7FFF) - 117*128; generated at build time by gen_silu_table.py.
 __device__ const uint16_t k_silu_mid[kSiluEntries] = {
 #include "silu_mid_table.inc"
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
-// silu(g) rounded once to BF16 (returned as its binary32 value).
+// silu(g) rounded once to BF16, for the gates outside the table:
 //   |g| < 2^-10 : silu(g) = g/2 + g^2/4 - ..., so the result is g/2, and when
 //                 g/2 falls between two BF16 values the exact value lies
 //                 above the midpoint: round toward +inf.
 //   g >= 8      : the relative gap g - silu(g) < e^-8 < 2^-9: the result is g.
 //   g <= -128   : |silu(g)| < 2^-134: the result is -0.
 //   +inf -> +inf, -inf and NaN -> NaN (a non-finite gate stays non-finite).
-//   otherwise   : table.
-__device__ __forceinline__ float silu_bf16(uint32_t g, const uint16_t* tab) {
-  const uint32_t e = (g >> 7) & 0xFFu;
+__device__ __noinline__ float silu_outside_table(uint32_t g) {
+  const uint32_t mag = g & 0x7FFFu;
   const uint32_t neg = g >> 15;
   uint32_t out;
-  if (e < 117u) {
+  if (mag < 117u * 128u) {
     const uint32_t u = __float_as_uint(bf16_to_f32(g) * 0.5f);  // exact, no flush to zero
     out = (u + (neg ? 0x7FFFu : 0x8000u)) >> 16;
-  } else if (e == 0xFFu) {
+  } else if (mag >= 0x7F80u) {
     out = (g == 0x7F80u) ? 0x7F80u : 0x7FC0u;
-  } else if (!neg) {
-    out = (e >= 130u) ? g : tab[(e - 117u) * 128u + (g & 0x7Fu)];
   } else {
-    out = (e >= 134u) ? 0x8000u : tab[1664u + (e - 117u) * 128u + (g & 0x7Fu)];
+    out = neg ? 0x8000u : g;
   }
   return bf16_to_f32(out);
 }
 
-// h = bf16(silu_bf16(g) * u): the binary32 product of two BF16 values is
-// exact, so this is a single rounding.
-__device__ __forceinline__ float swiglu(uint32_t g, uint32_t u, const uint16_t* tab) {
-  const float p = __fmul_rn(silu_bf16(g, tab), bf16_to_f32(u));
-  return __bfloat162float(__float2bfloat16_rn(p));
+// silu(g) rounded once to BF16 (returned as its binary32 value); the common
+// case is one shared-memory load from the table (entries stored as binary32).
+__device__ __forceinline__ float silu_bf16(uint32_t g, const float* tab) {
+  const uint32_t rel = (g & 0x7FFFu) - 117u * 128u;
+  const bool neg = (g & 0x8000u) != 0;
+  if (rel < (neg ? 2176u : 1664u)) return tab[rel + (neg ? 1664u : 0u)];
+  return silu_outside_table(g);
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
-  return __ldcs(reinterpret_cast<const uint4*>(p));
+// The exact binary32 product silu_bf16(g) * u (two BF16 significands: no
+// rounding); h = RNE_bf16 of it.
+__device__ __forceinline__ float swiglu_product(uint32_t g, uint32_t u, const float* tab) {
+  return __fmul_rn(silu_bf16(g, tab), bf16_to_f32(u));
 }
 
-// Eight h values of lane-chunk (row, c0).
-template <bool kSwiglu>
-__device__ __forceinline__ void load_h(const uint16_t* row, int64_t cols, int64_t c0, const uint16_t* tab,
-                                       float h[8]) {
-  const uint4 gv = ld_stream(row + c0);
-  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-  if constexpr (kSwiglu) {
-    const uint4 uv = ld_stream(row + cols + c0);
-    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      h[2 * i] = swiglu(gw[i] & 0xFFFFu, uw[i] & 0xFFFFu, tab);
-      h[2 * i + 1] = swiglu(gw[i] >> 16, uw[i] >> 16, tab);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      h[2 * i] = bf16_to_f32(gw[i] & 0xFFFFu);
-      h[2 * i + 1] = bf16_to_f32(gw[i] >> 16);
-    }
-  }
+// Two SwiGLU outputs as BF16 bits (lo in bits 0..15).
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw, const float* tab) {
+  return bf16x2_rn(swiglu_product(gw & 0xFFFFu, uw & 0xFFFFu, tab), swiglu_product(gw >> 16, uw >> 16, tab));
 }
 
 template <bool kSwiglu>
-__device__ __forceinline__ void load_table(uint16_t* tab) {
+__device__ __forceinline__ void load_table(float* tab) {
   if constexpr (kSwiglu) {
-    for (int i = threadIdx.x; i < kSiluEntries; i += blockDim.x) tab[i] = k_silu_mid[i];
+    for (int i = threadIdx.x; i < kSiluEntries; i += blockDim.x) tab[i] = bf16_to_f32(k_silu_mid[i]);
     __syncthreads();
   }
+}
+
+// Raw 16-element slice of one lane: 2 x 16 B of gate (or W) and, with
+// SwiGLU, 2 x 16 B of up.
+struct Slice {
+  uint4 g[2];
+  uint4 u[2];
+};
+
+template <bool kSwiglu, bool kStream>
+__device__ __forceinline__ void load_slice(const uint16_t* row, int64_t cols, int64_t c0, Slice& s) {
+  const uint4* pg = reinterpret_cast<const uint4*>(row + c0);
+  if constexpr (kStream) {
+    s.g[0] = __ldcs(pg);
+    s.g[1] = __ldcs(pg + 1);
+  } else {
+    s.g[0] = __ldg(pg);
+    s.g[1] = __ldg(pg + 1);
+  }
+  if constexpr (kSwiglu) {
+    const uint4* pu = reinterpret_cast<const uint4*>(row + cols + c0);
+    if constexpr (kStream) {
+      s.u[0] = __ldcs(pu);
+      s.u[1] = __ldcs(pu + 1);
+    } else {
+      s.u[0] = __ldg(pu);
+      s.u[1] = __ldg(pu + 1);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t word(const Slice& s, int i, bool up) {
+  const uint4& v = up ? s.u[i >> 2] : s.g[i >> 2];
+  return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+}
+
+// max |h| of a slice as a binary32 bit pattern.  With SwiGLU the exact
+// products are compared and the largest is rounded to BF16 once: rounding is
+// monotone, so max |RNE(p)| = RNE(max |p|).  Integer max keeps NaN (its bit
+// patterns sort above +inf).
+template <bool kSwiglu>
+__device__ __forceinline__ uint32_t slice_absmax_bits(const Slice& s, const float* tab) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t gw = word(s, i, false);
+    if constexpr (kSwiglu) {
+      const uint32_t uw = word(s, i, true);
+      m = max(m, __float_as_uint(swiglu_product(gw & 0xFFFFu, uw & 0xFFFFu, tab)) & 0x7FFFFFFFu);
+      m = max(m, __float_as_uint(swiglu_product(gw >> 16, uw >> 16, tab)) & 0x7FFFFFFFu);
+    } else {
+      m = max(m, (gw << 16) & 0x7FFFFFFFu);
+      m = max(m, gw & 0x7FFF0000u);
+    }
+  }
+  return m;
+}
+
+__device__ __forceinline__ uint32_t round_max_to_bf16(uint32_t m) {
+  if (m >= 0x7F800000u) return m;  // Inf / NaN stay as they are
+  return bf16x2_rn(__uint_as_float(m), 0.0f) << 16;
 }
 
 // Walks the units (row, segment) of a [rows, cols] grid, grid-strided over
@@ -129,25 +175,32 @@ struct UnitWalker {
 };
 
 // Pass 1: rec->amax_bits = max over the tensor of the bit pattern of |h|.
+// Two units in flight per warp.  Loads keep the default L2 policy so the
+// tail of the tensor is still in L2 when pass 2 (which walks backwards)
+// starts.
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kThreads) k_amax(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                                                    int64_t ld, nvfp4_scale_rec* rec) {
-  __shared__ uint16_t tab[kSwiglu ? kSiluEntries : 1];
+  __shared__ float tab[kSwiglu ? kSiluEntries : 1];
   __shared__ uint32_t wmax[kWarps];
   load_table<kSwiglu>(tab);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t segs = (cols + 255) / 256;
+  const int64_t segs = (cols + kSegElems - 1) / kSegElems;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
   uint32_t amax = 0;
-  for (UnitWalker w(first, stride, segs); w.row < rows; w.next()) {
-    const int64_t c0 = w.seg * 256 + lane * 8;
-    if (c0 < cols) {
-      float h[8];
-      load_h<kSwiglu>(x + w.row * ld, cols, c0, tab, h);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = max(amax, __float_as_uint(h[i]) & 0x7FFFFFFFu);
-    }
+  UnitWalker w(first, stride, segs);
+  while (w.row < rows) {
+    const int64_t r0 = w.row, c0 = w.seg * kSegElems + lane * 16;
+    w.next();
+    const int64_t r1 = w.row, c1 = w.seg * kSegElems + lane * 16;
+    w.next();
+    Slice s0, s1;
+    const bool v0 = c0 < cols, v1 = r1 < rows && c1 < cols;
+    if (v0) load_slice<kSwiglu, false>(x + r0 * ld, cols, c0, s0);
+    if (v1) load_slice<kSwiglu, false>(x + r1 * ld, cols, c1, s1);
+    if (v0) amax = max(amax, slice_absmax_bits<kSwiglu>(s0, tab));
+    if (v1) amax = max(amax, slice_absmax_bits<kSwiglu>(s1, tab));
   }
   amax = __reduce_max_sync(0xFFFFFFFFu, amax);
   if (lane == 0) wmax[warp] = amax;
@@ -156,16 +209,36 @@ __global__ void __launch_bounds__(kThreads) k_amax(const uint16_t* __restrict__ 
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) m = max(m, wmax[i]);
+    if constexpr (kSwiglu) m = round_max_to_bf16(m);
     if (m != 0) atomicMax(&rec->amax_bits, m);
   }
 }
 
-// Pass 2: quantise.  Units cover rows [0, rows_pad); rows >= rows are zeros.
+// True when q is within 3 units in the last place of a binary32 number with
+// at most `sig` significant bits (every rounding boundary of a format with
+// sig-1 fraction bits is such a number).  Used to send the rare quotients
+// whose rounding a multiply-by-reciprocal could get wrong to a true division.
+template <int kSig>
+__device__ __forceinline__ bool near_boundary(float q) {
+  constexpr uint32_t mask = (1u << (24 - kSig)) - 1u;
+  return ((__float_as_uint(q) + 3u) & mask) <= 6u;
+}
+
+// Block scale code of a block with max |h| = bmax: E4M3(RN(bmax / d)).
+__device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float rd) {
+  if (d == 0.0f) return 0u;
+  float r = __fmul_rn(bmax, rd);
+  if (near_boundary<5>(r)) r = __fdiv_rn(bmax, d);
+  return e4m3_code(r);
+}
+
+// Pass 2: quantise.  Units cover rows [0, rows_pad), walked from the end so
+// that the first reads hit what pass 1 left in L2; rows >= rows are zeros.
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                                                     int64_t ld, int64_t rows_pad, uint8_t* __restrict__ qdata,
                                                     uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
-  __shared__ uint16_t tab[kSwiglu ? kSiluEntries : 1];
+  __shared__ float tab[kSwiglu ? kSiluEntries : 1];
   load_table<kSwiglu>(tab);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
@@ -173,47 +246,69 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__
   const bool finite = amax_bits < 0x7F800000u;
   const float g = finite ? __fdiv_rn(__uint_as_float(amax_bits), 2688.0f) : __uint_as_float(0x7FC00000u);
   const float d = __fmul_rn(6.0f, g);
+  const float rd = (d == 0.0f || !finite) ? 0.0f : __frcp_rn(d);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     rec->global_scale = g;
     rec->status = finite ? NVFP4_OK : NVFP4_ENONFINITE;
   }
 
-  const int64_t segs = (cols + 255) / 256;
-  const int64_t nblk = cols / 16;
-  const int64_t cpad4 = (nblk + 3) / 4;  // 4-column groups per row (= tiles per 128-row block)
+  const int64_t segs = (cols + kSegElems - 1) / kSegElems;
+  const int64_t cpad4 = (cols / 16 + 3) / 4;  // 4-column scale groups per row
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
   for (UnitWalker w(first, stride, segs); w.row < rows_pad; w.next()) {
-    const int64_t r = w.row;
-    const int64_t c0 = w.seg * 256 + lane * 8;
+    const int64_t r = rows_pad - 1 - w.row;
+    const int64_t seg = segs - 1 - w.seg;
+    const int64_t c0 = seg * kSegElems + lane * 16;
     const bool valid = c0 < cols;
-    float h[8];
+    uint32_t hw[8];  // 16 BF16 values of h, two per word
     if (valid && finite && r < rows) {
-      load_h<kSwiglu>(x + r * ld, cols, c0, tab, h);
+      Slice s;
+      load_slice<kSwiglu, true>(x + r * ld, cols, c0, s);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(word(s, i, false), word(s, i, true), tab)
+                                                  : word(s, i, false);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = 0.0f;
+      for (int i = 0; i < 8; ++i) hw[i] = 0u;
     }
-    float lmax = 0.0f;
+    uint32_t mbits = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lmax = fmaxf(lmax, fabsf(h[i]));
-    const float bmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, 1));
-    const float ratio = (d == 0.0f) ? 0.0f : __fdiv_rn(bmax, d);
-    const uint32_t bs = finite ? e4m3_code(ratio) : 0u;
-    const float s = __fmul_rn(e4m3_value(bs), g);
-    uint32_t packed = 0;
-    if (s != 0.0f && finite) {
+    for (int i = 0; i < 8; ++i) mbits = max(mbits, max((hw[i] << 16) & 0x7FFFFFFFu, hw[i] & 0x7FFF0000u));
+    const uint32_t bs = finite ? block_scale_code(__uint_as_float(mbits), d, rd) : 0u;
+    const float sc = __fmul_rn(e4m3_value(bs), g);
+    uint2 packed = make_uint2(0u, 0u);
+    if (sc != 0.0f && finite) {
+      const float rs = __frcp_rn(sc);
+      float q[16];
+      bool near = false;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) packed |= e2m1_code(__fdiv_rn(h[i], s)) << (4 * i);
+      for (int i = 0; i < 8; ++i) {
+        q[2 * i] = __fmul_rn(bf16_to_f32(hw[i] & 0xFFFFu), rs);
+        q[2 * i + 1] = __fmul_rn(__uint_as_float(hw[i] & 0xFFFF0000u), rs);
+        near |= near_boundary<3>(q[2 * i]) | near_boundary<3>(q[2 * i + 1]);
+      }
+      if (near) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          q[2 * i] = __fdiv_rn(bf16_to_f32(hw[i] & 0xFFFFu), sc);
+          q[2 * i + 1] = __fdiv_rn(__uint_as_float(hw[i] & 0xFFFF0000u), sc);
+        }
+      }
+      uint32_t b[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = e2m1x2_code(q[2 * i], q[2 * i + 1]);
+      packed.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+      packed.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
     }
-    if (valid) *reinterpret_cast<uint32_t*>(qdata + r * (cols / 2) + c0 / 2) = packed;
+    if (valid) *reinterpret_cast<uint2*>(qdata + r * (cols / 2) + c0 / 2) = packed;
 
-    // scales: lanes 8j, 8j+2, 8j+4, 8j+6 hold blocks 4j..4j+3 of this segment
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
-    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 4);
-    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 6);
-    const int64_t grp = w.seg * 4 + (lane >> 3);  // 4-column group index
-    if ((lane & 7) == 0 && grp < cpad4) {
+    // scales: lanes 4j..4j+3 hold the four blocks of scale group j
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
+    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
+    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
+    const int64_t grp = seg * (kSegElems / 64) + (lane >> 2);
+    if ((lane & 3) == 0 && grp < cpad4) {
       const int64_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
       *reinterpret_cast<uint32_t*>(scales + off) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
@@ -263,23 +358,38 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
 // ---- diagnostics: the same device functions on test-chosen inputs ----------
 
 __global__ void k_diag_silu_all(uint16_t* out) {
-  __shared__ uint16_t tab[kSiluEntries];
+  __shared__ float tab[kSiluEntries];
   load_table<true>(tab);
   for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < 65536u; g += gridDim.x * blockDim.x)
     out[g] = static_cast<uint16_t>(__float_as_uint(silu_bf16(g, tab)) >> 16);
 }
 
+// SwiGLU through the producer's pass-2 path (swiglu_pair) and, for the
+// pass-1 path, the BF16 rounding of the exact product.
 __global__ void k_diag_swiglu(const uint16_t* gate, const uint16_t* up, uint16_t* h, int64_t n) {
-  __shared__ uint16_t tab[kSiluEntries];
+  __shared__ float tab[kSiluEntries];
   load_table<true>(tab);
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    h[i] = static_cast<uint16_t>(__float_as_uint(swiglu(gate[i], up[i], tab)) >> 16);
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t pair = swiglu_pair(gate[i] | (uint32_t(gate[i]) << 16), up[i] | (uint32_t(up[i]) << 16), tab);
+    const uint32_t p1 = round_max_to_bf16(__float_as_uint(swiglu_product(gate[i], up[i], tab)) & 0x7FFFFFFFu) >> 16;
+    const uint32_t lo = pair & 0xFFFFu, hi = pair >> 16;
+    // both halves of the pair and |pass-1 value| must agree; a disagreement
+    // is reported as the NaN pattern 0x7FFF, which never equals the oracle
+    const bool ok = lo == hi && ((lo & 0x7FFFu) == p1 || ((lo & 0x7FFFu) > 0x7F80u && p1 > 0x7F80u));
+    h[i] = static_cast<uint16_t>(ok ? lo : 0x7FFFu);
+  }
 }
 
 __device__ __forceinline__ uint32_t diag_code(int which, uint32_t bits) {
   const float f = __uint_as_float(bits);
-  return which == 0 ? e2m1_code(f) : e4m3_code(f);
+  if (which == 0) {
+    // the packed encoder in both slots; a slot disagreement shows up as an
+    // out-of-range code
+    const uint32_t lo = e2m1x2_code(f, 0.0f) & 0xFu, hi = e2m1x2_code(0.0f, f) >> 4;
+    return lo == hi ? lo : 0x100u | lo;
+  }
+  return e4m3_code(f);
 }
 
 __global__ void k_diag_transitions(int which, uint32_t* trans, uint32_t cap, uint32_t* count,
