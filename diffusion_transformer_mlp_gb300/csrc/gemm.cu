@@ -37,30 +37,37 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int BK_BYTES = 128;  // 256 E2M1 elements
-constexpr int STAGES = 5;
-constexpr int A_BYTES = BM * BK_BYTES;
-constexpr int B_BYTES = BN * BK_BYTES;
-constexpr int SF_BYTES = 2048;  // 128 rows x 16 scales (four 512-byte 128x4 tiles)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
+// Tile of one CTA pair: 256 rows of A x 256 rows of W (256 x 256 outputs);
+// each CTA holds 128 rows of A and 128 rows of W per stage and 128 x 256
+// FP32 accumulators in its tensor memory.
+constexpr int PAIR_M = 256;
+constexpr int PAIR_N = 256;
+constexpr int HALF = 128;
+constexpr int BK_BYTES = 128;  // 256 E2M1 elements per k-tile
+constexpr int STAGES = 4;
+constexpr int A_BYTES = HALF * BK_BYTES;       // 16 KB
+constexpr int B_BYTES = HALF * BK_BYTES;       // 16 KB
+constexpr int SFA_BYTES = 2048;                // this CTA's 128 rows x 16 scales
+constexpr int SFB_BYTES = 4096;                // all 256 W rows x 16 scales
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
 constexpr int EPI_WARPS = 4;
-constexpr int EPI_BYTES = EPI_WARPS * 32 * BN * 2;  // per warp: 32 rows x 128 BF16
+constexpr int EPI_BYTES = HALF * PAIR_N * 2;   // 128 rows x 256 BF16
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;    // two 128-column FP32 accumulators
-constexpr uint32_t SF_COL = 256;   // per stage: 16 columns of A scales, 16 of W scales
-static_assert(SF_COL + STAGES * 32 <= TMEM_COLS, "tensor memory budget");
+constexpr uint32_t ACC_COL = 0;     // 256 FP32 columns
+constexpr uint32_t SF_COL = 256;    // per stage: 16 columns of A scales, 32 of W scales
+constexpr uint32_t SF_STAGE_COLS = 48;
+static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment for 128B swizzle");
 
 // Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), both
 // K-major, UE4M3 scales (scale format 0), scale-factor ids 0, N>>3 at bit
-// 17, M>>4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// 17, M>>4 at bit 24; M = 256 across the CTA pair.
+constexpr uint32_t kIdesc =
+    (1u << 7) | (1u << 10) | (uint32_t(PAIR_N >> 3) << 17) | (uint32_t(PAIR_M >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major operand tile whose rows are
 // 128 bytes with the 128-byte swizzle: 8-row atoms 1024 bytes apart (SBO),
@@ -77,11 +84,11 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 
 struct Smem {
   uint8_t* stage;  // STAGES x [A | B | SFA | SFB]
-  uint8_t* epi;    // EPI_WARPS x 8 KB
-  uint64_t* full;
+  uint8_t* epi;    // EPI_WARPS x 32 rows x 256 BF16
+  uint64_t* full;  // used in the leader CTA only
   uint64_t* empty;
   uint64_t* tfull;
-  uint64_t* tempty;
+  uint64_t* tempty;  // used in the leader CTA only
   uint64_t* mma_done;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -96,22 +103,24 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.full = bars;
   s.empty = bars + STAGES;
   s.tfull = bars + 2 * STAGES;
-  s.tempty = bars + 2 * STAGES + 2;
-  s.mma_done = bars + 2 * STAGES + 4;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  s.tempty = bars + 2 * STAGES + 1;
+  s.mma_done = bars + 2 * STAGES + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
 }
 
 struct Params {
-  const uint8_t* a_s;
-  const uint8_t* w_s;
   const nvfp4_scale_rec* a_rec;
   const nvfp4_scale_rec* w_rec;
-  int num_m_tiles, num_n_tiles, num_k_tiles;
-  int64_t sf_panel_bytes;  // bytes of scales per 128-row panel: (C4/4) * 512
+  int a_rows;       // padded rows of the activation (multiple of 128)
+  int n;            // weight rows (multiple of 128)
+  int num_m_tiles;  // ceil(a_rows / 256)
+  int num_n_tiles;  // ceil(n / 256)
+  int num_k_tiles;  // k / 256
+  int sf_panel_rows;  // rows of 256 B per 128-row scale panel: (k/64) * 512 / 256
   uint32_t* dev_status;
-  uint64_t wait_limit_ns;
+  uint64_t wait_limit_cycles;
 };
 
 __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag) {
@@ -119,12 +128,27 @@ __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag)
   if (p.dev_status != nullptr) atomicExch(p.dev_status, static_cast<uint32_t>(NVFP4_ETIMEOUT));
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// Bytes one CTA of the pair loads per k-tile for tile (mt, nt): halves that
+// fall outside the operands are not loaded (their rows are never stored).
+__device__ __forceinline__ uint32_t cta_stage_bytes(const Params& p, int mt, int nt, uint32_t rank) {
+  uint32_t b = 0;
+  if (mt * PAIR_M + int(rank) * HALF < p.a_rows) b += A_BYTES + SFA_BYTES;
+  if (nt * PAIR_N + int(rank) * HALF < p.n) b += B_BYTES;
+  b += SFB_BYTES / 2;                                   // W scales of rows 0..127 of the tile
+  if (nt * PAIR_N + HALF < p.n) b += SFB_BYTES / 2;     // rows 128..255
+  return b;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+               const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
                const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   const volatile int* abort_flag = sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -132,81 +156,81 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.tfull[b], 1);
-      mbar_init(&sm.tempty[b], EPI_WARPS);
-    }
+    mbar_init(sm.tfull, 1);
+    mbar_init(sm.tempty, 2 * EPI_WARPS);
     mbar_init(sm.mma_done, 1);
     *sm.abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_sa);
+    prefetch_tmap(&tmap_sw);
     prefetch_tmap(&tmap_out);
   }
-  if (warp == 1) tmem_alloc(sm.tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated in both
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_last();
       const uint64_t pol_a = l2_policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_parity = 0;  // last issued phase per stage
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const int mb = t / p.num_n_tiles, nb = t - (t / p.num_n_tiles) * p.num_n_tiles;
-        const uint8_t* sfa = p.a_s + mb * p.sf_panel_bytes;
-        const uint8_t* sfw = p.w_s + nb * p.sf_panel_bytes;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
+        const int a_row = mt * PAIR_M + int(rank) * HALF;
+        const int b_row = nt * PAIR_N + int(rank) * HALF;
+        const bool a_ok = a_row < p.a_rows, b_ok = b_row < p.n, b1_ok = nt * PAIR_N + HALF < p.n;
+        const uint32_t tx = cta_stage_bytes(p, mt, nt, 0) + cta_stage_bytes(p, mt, nt, 1);
+        const int sfa_row0 = (a_row / HALF) * p.sf_panel_rows;
+        const int sfb_row0 = (nt * 2) * p.sf_panel_rows;
         for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-          if (!mbar_wait_bounded(&sm.empty[stage], phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+          if (!mbar_wait_bounded(&sm.empty[stage], phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
             break;
           }
           uint8_t* st = sm.stage + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&sm.full[stage], STAGE_BYTES);
-          tma_load_2d(st, &tmap_a, &sm.full[stage], kt * BK_BYTES, mb * BM, pol_a);
-          tma_load_2d(st + A_BYTES, &tmap_w, &sm.full[stage], kt * BK_BYTES, nb * BN, pol_w);
-          bulk_load(st + A_BYTES + B_BYTES, sfa + kt * SF_BYTES, SF_BYTES, &sm.full[stage], pol_a);
-          bulk_load(st + A_BYTES + B_BYTES + SF_BYTES, sfw + kt * SF_BYTES, SF_BYTES, &sm.full[stage], pol_w);
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&sm.full[stage], tx);
+          if (a_ok) {
+            tma_load_2d_pair(st, &tmap_a, full_leader, kt * BK_BYTES, a_row, pol_a);
+            tma_load_2d_pair(st + A_BYTES + B_BYTES, &tmap_sa, full_leader, 0, sfa_row0 + kt * 8, pol_a);
+          }
+          if (b_ok) tma_load_2d_pair(st + A_BYTES, &tmap_w, full_leader, kt * BK_BYTES, b_row, pol_w);
+          uint8_t* sfb = st + A_BYTES + B_BYTES + SFA_BYTES;
+          tma_load_2d_pair(sfb, &tmap_sw, full_leader, 0, sfb_row0 + kt * 8, pol_w);
+          if (b1_ok) tma_load_2d_pair(sfb + SFB_BYTES / 2, &tmap_sw, full_leader, 0, sfb_row0 + p.sf_panel_rows + kt * 8,
+                                      pol_w);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Every copy this thread issued must have landed before the CTA exits
-      // (they have, on the normal path: the MMA warp consumed them).
-      for (int s = 0; s < STAGES; ++s)
-        if (issued_mask & (1u << s))
-          if (!mbar_wait_bounded(&sm.full[s], (issued_parity >> s) & 1u, p.wait_limit_ns, nullptr))
-            report_timeout(p, sm.abort_flag);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-        const uint32_t acc = local & 1;
-        if (!mbar_wait_bounded(&sm.tempty[acc], ((local >> 1) & 1) ^ 1u, p.wait_limit_ns, abort_flag)) {
+      for (int t = pair; t < num_tiles && ok; t += num_pairs, ++local) {
+        if (!mbar_wait_bounded(sm.tempty, (local & 1) ^ 1u, p.wait_limit_cycles, abort_flag)) {
           report_timeout(p, sm.abort_flag);
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + ACC_COL + acc * BN;
         for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-          if (!mbar_wait_bounded(&sm.full[stage], phase, p.wait_limit_ns, abort_flag)) {
+          if (!mbar_wait_bounded(&sm.full[stage], phase, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
             break;
@@ -215,58 +239,57 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint8_t* st = sm.stage + stage * STAGE_BYTES;
           const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + A_BYTES);
           const uint32_t sfa_addr = smem_u32(st + A_BYTES + B_BYTES);
-          const uint32_t sfb_addr = sfa_addr + SF_BYTES;
-          const uint32_t sf_tmem = tmem + SF_COL + stage * 32;
+          const uint32_t sfb_addr = sfa_addr + SFA_BYTES;
+          const uint32_t sfa_tmem = tmem + SF_COL + stage * SF_STAGE_COLS;
+          const uint32_t sfb_tmem = sfa_tmem + 16;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_warpx4(sf_tmem + 4 * j, desc_sf(sfa_addr + 512 * j));
-            tc_cp_32x128b_warpx4(sf_tmem + 16 + 4 * j, desc_sf(sfb_addr + 512 * j));
+            tc_cp_pair_32x128b_warpx4(sfa_tmem + 4 * j, desc_sf(sfa_addr + 512 * j));
+            tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j, desc_sf(sfb_addr + 512 * j));
+            tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j + 4, desc_sf(sfb_addr + SFB_BYTES / 2 + 512 * j));
           }
           const uint64_t a_desc = desc_sw128(a_addr), b_desc = desc_sw128(b_addr);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // K step j: 64 elements = 32 bytes further along the swizzled row
-            tc_mma_nvf4(d_tmem, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sf_tmem + 4 * j, sf_tmem + 16 + 4 * j,
-                        (kt | j) != 0);
+            tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sfa_tmem + 4 * j,
+                             sfb_tmem + 8 * j, (kt | j) != 0);
           }
-          tc_commit(&sm.empty[stage]);  // frees the stage once these MMAs complete
+          tc_commit_pair(&sm.empty[stage]);  // frees the stage in both CTAs once these MMAs complete
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&sm.tfull[acc]);  // accumulator ready once all MMAs complete
+        tc_commit_pair(sm.tfull);  // accumulators of both CTAs ready
       }
       // Nothing may still be reading shared memory or writing tensor memory
-      // when the CTA tears down.
-      tc_commit(sm.mma_done);
-      if (!mbar_wait_bounded(sm.mma_done, 0, p.wait_limit_ns, nullptr)) report_timeout(p, sm.abort_flag);
+      // in either CTA when the pair tears down.
+      tc_commit_pair(sm.mma_done);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
-    uint8_t* stg = sm.epi + q * (32 * BN * 2);
+    uint8_t* stg = sm.epi + q * (32 * PAIR_N * 2);
+    const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      const int mb = t / p.num_n_tiles, nb = t - (t / p.num_n_tiles) * p.num_n_tiles;
-      const uint32_t acc = local & 1;
-      // one lane waits, the warp follows its verdict (tcgen05.ld is warp-wide)
+    for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
+      const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(&sm.tfull[acc], (local >> 1) & 1, p.wait_limit_ns, abort_flag);
+      if (lane == 0) ok = mbar_wait_bounded(sm.tfull, local & 1, p.wait_limit_cycles, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) {
         if (lane == 0) report_timeout(p, sm.abort_flag);
         break;
       }
       tc_fence_after();
-      // the previous TMA store must have finished reading the staging buffer
-      if (lane == 0) bulk_wait_read_all();
+      if (lane == 0) bulk_wait_read_all();  // previous stores have read the staging buffer
       __syncwarp();
-      const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL + acc * BN;
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
+      const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL;
+#pragma unroll 1
+      for (int c = 0; c < PAIR_N / 32; ++c) {
         uint32_t r[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -280,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             : "r"(row_tmem + c * 32));
         tc_wait_ld();
         // row `lane` of this quarter, columns 32c..32c+31 -> 4 chunks of 16 B
-        uint8_t* half = stg + (c >> 1) * (32 * 128) + lane * 128;
+        uint8_t* sub = stg + (c >> 1) * (32 * 128) + lane * 128;
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
           uint32_t w[4];
@@ -288,35 +311,44 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 4; ++i) {
             const float lo = __fmul_rn(__uint_as_float(r[t4 * 8 + 2 * i]), alpha);
             const float hi = __fmul_rn(__uint_as_float(r[t4 * 8 + 2 * i + 1]), alpha);
-            const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-            w[i] = *reinterpret_cast<const uint32_t*>(&v);
+            w[i] = bf16x2_rn(lo, hi);
           }
           const int chunk = ((c & 1) * 4 + t4) ^ (lane & 7);
-          *reinterpret_cast<uint4*>(half + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(sub + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      // accumulator drained: hand it back to the MMA warp
+      // accumulator drained: hand it back to the MMA issuer of the pair
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+      if (lane == 0) mbar_arrive_cluster(tempty_leader);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int y = mb * BM + q * 32;
-        tma_store_2d(&tmap_out, stg, nb * BN, y);
-        tma_store_2d(&tmap_out, stg + 32 * 128, nb * BN + 64, y);
+        const int y = mt * PAIR_M + int(rank) * HALF + q * 32;
+        if (y < p.a_rows) {
+#pragma unroll
+          for (int h = 0; h < PAIR_N / 64; ++h) {
+            const int x = nt * PAIR_N + h * 64;
+            if (x < p.n) tma_store_2d(&tmap_out, stg + h * (32 * 128), x, y);
+          }
+        }
         bulk_commit();
       }
     }
     if (lane == 0) bulk_wait_all();
   }
 
+  // teardown: every MMA of the pair has completed before tensor memory is freed
+  if (warp == 1 && lane == 0) {
+    if (!mbar_wait_bounded(sm.mma_done, 0, p.wait_limit_cycles, nullptr)) report_timeout(p, sm.abort_flag);
+  }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -342,7 +374,7 @@ EncodeTiledFn encode_fn() {
 
 nvfp4_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                         const char* what) {
+                         CUtensorMapSwizzle swizzle, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(NVFP4_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {inner, outer};
@@ -350,8 +382,7 @@ nvfp4_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* b
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[160];
     std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, int(r));
@@ -362,62 +393,75 @@ nvfp4_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* b
 
 }  // namespace
 
-// Default bounded-wait limit: far above any legitimate wait (a whole
-// canonical GEMM takes about a millisecond) yet short enough that a broken
-// pipeline returns control instead of holding the GPU.
-constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+// Default bounded-wait limit in SM cycles (about two seconds at the highest
+// clock): far above any legitimate wait (a whole canonical GEMM takes about a
+// millisecond) yet short enough that a broken pipeline returns control
+// instead of holding the GPU.
+constexpr uint64_t kDefaultWaitLimitCycles = 4000000000ull;
 
 nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec, const void* w_q,
                              const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m, int64_t n, int64_t k,
                              void* out, int64_t ldo, uint32_t* dev_status, cudaStream_t stream,
-                             uint64_t wait_limit_ns) {
+                             uint64_t wait_limit_cycles) {
   if (!a_q || !a_s || !a_rec || !w_q || !w_s || !w_rec || !out)
     return fail(NVFP4_EINVAL, "nvfp4_fc2_gemm: null pointer");
   if (m < 1) return fail(NVFP4_EINVAL, "nvfp4_fc2_gemm: m must be >= 1");
-  if (n < BN || n % BN != 0) return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: n must be a positive multiple of 128");
+  if (n < HALF || n % HALF != 0) return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: n must be a positive multiple of 128");
   if (k < 256 || k % 256 != 0) return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: k must be a positive multiple of 256");
   if (ldo < n) return fail(NVFP4_EINVAL, "nvfp4_fc2_gemm: ldo < n");
   if (ldo % 8 != 0 || !aligned16(a_q) || !aligned16(a_s) || !aligned16(w_q) || !aligned16(w_s) || !aligned16(out) ||
       !aligned16(a_rec) || !aligned16(w_rec))
     return fail(NVFP4_EALIGN, "nvfp4_fc2_gemm: pointers must be 16-byte aligned and ldo a multiple of 8");
   const int64_t m_pad = nvfp4_padded_rows(m);
-  if (m_pad / BM > (int64_t(1) << 24) || n > (int64_t(1) << 24) || k > (int64_t(1) << 24))
+  if (m_pad > (int64_t(1) << 30) || n > (int64_t(1) << 24) || k > (int64_t(1) << 24))
     return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: problem too large");
 
-  CUtensorMap ta, tw, to;
+  // Scales are fetched as 2 KB boxes of a [bytes / 256, 256] byte matrix:
+  // one 128-row panel x one k-tile (256 K) is 2,048 contiguous bytes.
+  const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256, sw_rows = nvfp4_scale_bytes(n, k) / 256;
+  CUtensorMap ta, tw, tsa, tsw, to;
   nvfp4_status st;
-  if ((st = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, k / 2, m_pad, k / 2, BK_BYTES, BM, "A")) != NVFP4_OK)
+  if ((st = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, k / 2, m_pad, k / 2, BK_BYTES, HALF,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) != NVFP4_OK)
     return st;
-  if ((st = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_q, k / 2, n, k / 2, BK_BYTES, BN, "W")) != NVFP4_OK)
+  if ((st = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_q, k / 2, n, k / 2, BK_BYTES, HALF,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "W")) != NVFP4_OK)
     return st;
-  if ((st = make_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, n, m, ldo * 2, 64, 32, "out")) != NVFP4_OK)
+  if ((st = make_map_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_s, 256, sa_rows, 256, 256, 8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, "A scales")) != NVFP4_OK)
+    return st;
+  if ((st = make_map_2d(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 256, sw_rows, 256, 256, 8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, "W scales")) != NVFP4_OK)
+    return st;
+  if ((st = make_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, n, m, ldo * 2, 64, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "out")) != NVFP4_OK)
     return st;
 
   Params prm;
-  prm.a_s = static_cast<const uint8_t*>(a_s);
-  prm.w_s = static_cast<const uint8_t*>(w_s);
   prm.a_rec = a_rec;
   prm.w_rec = w_rec;
-  prm.num_m_tiles = static_cast<int>(m_pad / BM);
-  prm.num_n_tiles = static_cast<int>(n / BN);
+  prm.a_rows = static_cast<int>(m_pad);
+  prm.n = static_cast<int>(n);
+  prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
+  prm.num_n_tiles = static_cast<int>((n + PAIR_N - 1) / PAIR_N);
   prm.num_k_tiles = static_cast<int>(k / 256);
-  prm.sf_panel_bytes = (k / 16 / 4) * 512;
+  prm.sf_panel_rows = static_cast<int>(k / 32);
   prm.dev_status = dev_status;
-  prm.wait_limit_ns = wait_limit_ns;
+  prm.wait_limit_cycles = wait_limit_cycles;
 
   st = cuda_check(cudaFuncSetAttribute(k_fc2_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES),
                   "cudaFuncSetAttribute(k_fc2_gemm)");
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  k_fc2_gemm<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tw, to, prm);
+  const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
+  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, to, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
 // ---- diagnostics: the bounded wait on a barrier nothing arrives at ---------
 
 namespace {
-__global__ void k_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status) {
+__global__ void k_diag_wait_timeout(uint64_t limit_cycles, uint32_t* dev_status) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -427,7 +471,7 @@ __global__ void k_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (!mbar_wait_bounded(&bar, 0, limit_ns, &abort_flag)) *dev_status = NVFP4_ETIMEOUT;
+    if (!mbar_wait_bounded(&bar, 0, limit_cycles, &abort_flag)) *dev_status = NVFP4_ETIMEOUT;
     else *dev_status = NVFP4_OK;
     mbar_arrive(&bar);  // complete the phase so the barrier is left idle
   }
@@ -443,12 +487,13 @@ extern "C" nvfp4_status nvfp4_fc2_gemm(const void* a_q, const void* a_s, const n
                                        int64_t n, int64_t k, void* out_bf16, int64_t ldo, uint32_t* dev_status,
                                        nvfp4_stream_t stream) {
   return fc2_gemm_launch(a_q, a_s, a_rec, w_q, w_s, w_rec, m, n, k, out_bf16, ldo, dev_status,
-                         reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitNs);
+                         reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitCycles);
 }
 
 extern "C" nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status, nvfp4_stream_t stream) {
   if (!dev_status || limit_ns < 1 || limit_ns > 1000000000ull)
     return fail(NVFP4_EINVAL, "nvfp4_diag_wait_timeout: bad arguments");
-  k_diag_wait_timeout<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, dev_status);
+  // cycles at the highest SM clock (2.07 GHz) give at least limit_ns of wall time
+  k_diag_wait_timeout<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns * 21 / 10, dev_status);
   return cuda_check(cudaGetLastError(), "launch k_diag_wait_timeout");
 }
