@@ -44,12 +44,15 @@ constexpr int PAIR_M = 256;
 constexpr int PAIR_N = 256;
 constexpr int HALF = 128;
 constexpr int BK_BYTES = 128;  // 256 E2M1 elements per k-tile
-constexpr int STAGES = 4;
-constexpr int A_BYTES = HALF * BK_BYTES;       // 16 KB
-constexpr int B_BYTES = HALF * BK_BYTES;       // 16 KB
-constexpr int SFA_BYTES = 2048;                // this CTA's 128 rows x 16 scales
-constexpr int SFB_BYTES = 4096;                // all 256 W rows x 16 scales
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
+constexpr int KT = 2;          // k-tiles per pipeline stage (one TMA box per operand per stage)
+constexpr int STAGES = 2;
+constexpr int KTILE_BYTES = HALF * BK_BYTES;   // 16 KB: 128 rows x one k-tile
+constexpr int A_BYTES = KT * KTILE_BYTES;      // this CTA's 128 A rows x KT k-tiles
+constexpr int B_BYTES = KT * KTILE_BYTES;      // this CTA's 128 W rows x KT k-tiles
+constexpr int SFA_BYTES = KT * 2048;           // this CTA's 128 rows x 16 scales per k-tile
+constexpr int SFB_PANEL = KT * 2048;           // one 128-row W panel
+constexpr int SFB_BYTES = 2 * SFB_PANEL;       // all 256 W rows of the tile
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 76 KB
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BYTES = HALF * PAIR_N * 2;   // 128 rows x 256 BF16
 constexpr int BAR_BYTES = 256;
@@ -57,8 +60,8 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;     // 256 FP32 columns
-constexpr uint32_t SF_COL = 256;    // per stage: 16 columns of A scales, 32 of W scales
-constexpr uint32_t SF_STAGE_COLS = 48;
+constexpr uint32_t SF_COL = 256;    // per stage and k-tile: 16 columns of A scales, 32 of W scales
+constexpr uint32_t SF_STAGE_COLS = 48 * KT;
 static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment for 128B swizzle");
@@ -117,8 +120,8 @@ struct Params {
   int n;            // weight rows (multiple of 128)
   int num_m_tiles;  // ceil(a_rows / 256)
   int num_n_tiles;  // ceil(n / 256)
-  int num_k_tiles;  // k / 256
-  int sf_panel_rows;  // rows of 256 B per 128-row scale panel: (k/64) * 512 / 256
+  int num_stages_k; // ceil(k / 256 / KT)
+  int sf_panel_rows;  // rows of 256 B per 128-row scale panel: k / 32
   uint32_t* dev_status;
   uint64_t wait_limit_cycles;
 };
@@ -126,17 +129,6 @@ struct Params {
 __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag) {
   *reinterpret_cast<volatile int*>(abort_flag) = 1;
   if (p.dev_status != nullptr) atomicExch(p.dev_status, static_cast<uint32_t>(NVFP4_ETIMEOUT));
-}
-
-// Bytes one CTA of the pair loads per k-tile for tile (mt, nt): halves that
-// fall outside the operands are not loaded (their rows are never stored).
-__device__ __forceinline__ uint32_t cta_stage_bytes(const Params& p, int mt, int nt, uint32_t rank) {
-  uint32_t b = 0;
-  if (mt * PAIR_M + int(rank) * HALF < p.a_rows) b += A_BYTES + SFA_BYTES;
-  if (nt * PAIR_N + int(rank) * HALF < p.n) b += B_BYTES;
-  b += SFB_BYTES / 2;                                   // W scales of rows 0..127 of the tile
-  if (nt * PAIR_N + HALF < p.n) b += SFB_BYTES / 2;     // rows 128..255
-  return b;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
@@ -185,13 +177,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
         const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
+        // Boxes beyond the operands (the last M or N half) are zero-filled by
+        // the TMA and still count their full bytes, so every stage carries
+        // 2 x STAGE_BYTES for the leader's barrier.
         const int a_row = mt * PAIR_M + int(rank) * HALF;
         const int b_row = nt * PAIR_N + int(rank) * HALF;
-        const bool a_ok = a_row < p.a_rows, b_ok = b_row < p.n, b1_ok = nt * PAIR_N + HALF < p.n;
-        const uint32_t tx = cta_stage_bytes(p, mt, nt, 0) + cta_stage_bytes(p, mt, nt, 1);
         const int sfa_row0 = (a_row / HALF) * p.sf_panel_rows;
-        const int sfb_row0 = (nt * 2) * p.sf_panel_rows;
-        for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+        for (int ks = 0; ks < p.num_stages_k; ++ks) {
           if (!mbar_wait_bounded(&sm.empty[stage], phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
@@ -199,16 +191,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           uint8_t* st = sm.stage + stage * STAGE_BYTES;
           const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&sm.full[stage], tx);
-          if (a_ok) {
-            tma_load_2d_pair(st, &tmap_a, full_leader, kt * BK_BYTES, a_row, pol_a);
-            tma_load_2d_pair(st + A_BYTES + B_BYTES, &tmap_sa, full_leader, 0, sfa_row0 + kt * 8, pol_a);
-          }
-          if (b_ok) tma_load_2d_pair(st + A_BYTES, &tmap_w, full_leader, kt * BK_BYTES, b_row, pol_w);
-          uint8_t* sfb = st + A_BYTES + B_BYTES + SFA_BYTES;
-          tma_load_2d_pair(sfb, &tmap_sw, full_leader, 0, sfb_row0 + kt * 8, pol_w);
-          if (b1_ok) tma_load_2d_pair(sfb + SFB_BYTES / 2, &tmap_sw, full_leader, 0, sfb_row0 + p.sf_panel_rows + kt * 8,
-                                      pol_w);
+          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * STAGE_BYTES);
+          tma_load_3d_pair(st, &tmap_a, full_leader, 0, a_row, ks * KT, pol_a);
+          tma_load_3d_pair(st + A_BYTES, &tmap_w, full_leader, 0, b_row, ks * KT, pol_w);
+          tma_load_2d_pair(st + A_BYTES + B_BYTES, &tmap_sa, full_leader, 0, sfa_row0 + ks * KT * 8, pol_a);
+          tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmap_sw, full_leader, 0, ks * KT * 8, nt * 2, pol_w);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -229,7 +216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+        for (int ks = 0; ks < p.num_stages_k; ++ks) {
           if (!mbar_wait_bounded(&sm.full[stage], phase, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
@@ -240,20 +227,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + A_BYTES);
           const uint32_t sfa_addr = smem_u32(st + A_BYTES + B_BYTES);
           const uint32_t sfb_addr = sfa_addr + SFA_BYTES;
-          const uint32_t sfa_tmem = tmem + SF_COL + stage * SF_STAGE_COLS;
-          const uint32_t sfb_tmem = sfa_tmem + 16;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_pair_32x128b_warpx4(sfa_tmem + 4 * j, desc_sf(sfa_addr + 512 * j));
-            tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j, desc_sf(sfb_addr + 512 * j));
-            tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j + 4, desc_sf(sfb_addr + SFB_BYTES / 2 + 512 * j));
-          }
-          const uint64_t a_desc = desc_sw128(a_addr), b_desc = desc_sw128(b_addr);
+          for (int kk = 0; kk < KT; ++kk) {
+            const uint32_t sfa_tmem = tmem + SF_COL + stage * SF_STAGE_COLS + kk * 48;
+            const uint32_t sfb_tmem = sfa_tmem + 16;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // K step j: 64 elements = 32 bytes further along the swizzled row
-            tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sfa_tmem + 4 * j,
-                             sfb_tmem + 8 * j, (kt | j) != 0);
+            for (int j = 0; j < 4; ++j) {
+              tc_cp_pair_32x128b_warpx4(sfa_tmem + 4 * j, desc_sf(sfa_addr + kk * 2048 + 512 * j));
+              tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j, desc_sf(sfb_addr + kk * 2048 + 512 * j));
+              tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j + 4, desc_sf(sfb_addr + SFB_PANEL + kk * 2048 + 512 * j));
+            }
+            const uint64_t a_desc = desc_sw128(a_addr + kk * KTILE_BYTES), b_desc = desc_sw128(b_addr + kk * KTILE_BYTES);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              // K step j: 64 elements = 32 bytes further along the swizzled row
+              tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sfa_tmem + 4 * j,
+                               sfb_tmem + 8 * j, (ks | kk | j) != 0);
+            }
           }
           tc_commit_pair(&sm.empty[stage]);  // frees the stage in both CTAs once these MMAs complete
           if (++stage == STAGES) {
@@ -372,17 +362,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-nvfp4_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                         CUtensorMapSwizzle swizzle, const char* what) {
+nvfp4_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int rank, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(NVFP4_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, dt, cuuint32_t(rank), const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[160];
     std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, int(r));
@@ -416,26 +403,53 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   if (m_pad > (int64_t(1) << 30) || n > (int64_t(1) << 24) || k > (int64_t(1) << 24))
     return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: problem too large");
 
-  // Scales are fetched as 2 KB boxes of a [bytes / 256, 256] byte matrix:
-  // one 128-row panel x one k-tile (256 K) is 2,048 contiguous bytes.
-  const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256, sw_rows = nvfp4_scale_bytes(n, k) / 256;
+  // A and W: 3-D views [k-tile][row][128 B] so one box carries KT k-tiles of
+  // 128 rows (each a 128B-swizzled 16 KB tile).  Scales: [bytes / 256, 256]
+  // byte rows (one 128-row panel x one k-tile is 8 rows = 2 KB); the W scales
+  // as [panel][row][256] so one box carries both panels of a 256-row tile.
+  const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256;
   CUtensorMap ta, tw, tsa, tsw, to;
   nvfp4_status st;
-  if ((st = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, k / 2, m_pad, k / 2, BK_BYTES, HALF,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) != NVFP4_OK)
-    return st;
-  if ((st = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_q, k / 2, n, k / 2, BK_BYTES, HALF,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "W")) != NVFP4_OK)
-    return st;
-  if ((st = make_map_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_s, 256, sa_rows, 256, 256, 8,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, "A scales")) != NVFP4_OK)
-    return st;
-  if ((st = make_map_2d(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 256, sw_rows, 256, 256, 8,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, "W scales")) != NVFP4_OK)
-    return st;
-  if ((st = make_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, n, m, ldo * 2, 64, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "out")) != NVFP4_OK)
-    return st;
+  {
+    const cuuint64_t dims[3] = {128, cuuint64_t(m_pad), cuuint64_t(k / 256)};
+    const cuuint64_t strides[2] = {cuuint64_t(k / 2), 128};
+    const cuuint32_t box[3] = {BK_BYTES, HALF, KT};
+    if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                       "A")) != NVFP4_OK)
+      return st;
+  }
+  {
+    const cuuint64_t dims[3] = {128, cuuint64_t(n), cuuint64_t(k / 256)};
+    const cuuint64_t strides[2] = {cuuint64_t(k / 2), 128};
+    const cuuint32_t box[3] = {BK_BYTES, HALF, KT};
+    if ((st = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                       "W")) != NVFP4_OK)
+      return st;
+  }
+  {
+    const cuuint64_t dims[2] = {256, cuuint64_t(sa_rows)};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {256, 8 * KT};
+    if ((st = make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_s, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       "A scales")) != NVFP4_OK)
+      return st;
+  }
+  {
+    const cuuint64_t dims[3] = {256, cuuint64_t(k / 32), cuuint64_t(n / 128)};
+    const cuuint64_t strides[2] = {256, cuuint64_t(k / 32) * 256};
+    const cuuint32_t box[3] = {256, 8 * KT, 2};
+    if ((st = make_map(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       "W scales")) != NVFP4_OK)
+      return st;
+  }
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(n), cuuint64_t(m)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldo) * 2};
+    const cuuint32_t box[2] = {64, 32};
+    if ((st = make_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                       "out")) != NVFP4_OK)
+      return st;
+  }
 
   Params prm;
   prm.a_rec = a_rec;
@@ -444,7 +458,9 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
   prm.num_n_tiles = static_cast<int>((n + PAIR_N - 1) / PAIR_N);
-  prm.num_k_tiles = static_cast<int>(k / 256);
+  // an odd k-tile count ends with a box whose second k-tile lies beyond K:
+  // the TMA fills it with zeros, which add nothing to the sums
+  prm.num_stages_k = static_cast<int>((k / 256 + KT - 1) / KT);
   prm.sf_panel_rows = static_cast<int>(k / 32);
   prm.dev_status = dev_status;
   prm.wait_limit_cycles = wait_limit_cycles;
