@@ -54,26 +54,15 @@ constexpr int SFB_PANEL = KT * 2048;           // one 128-row W panel
 constexpr int SFB_BYTES = 2 * SFB_PANEL;       // all 256 W rows of the tile
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 76 KB
 constexpr int EPI_WARPS = 4;
-constexpr int SF_WARPS = 4;
 constexpr int EPI_BYTES = HALF * PAIR_N * 2;   // 128 rows x 256 BF16
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-constexpr int THREADS = 64 + (EPI_WARPS + SF_WARPS) * 32;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;     // 256 FP32 columns
-// Scale factors in tensor memory, per stage (8 K=64 steps):
-//   A: step j at column SFA + 4j; the scales of accumulator row i are read
-//      from lane i, column SFA + 4j + i/32 (32 columns per stage).
-//   W: step j at column SFB + 8j; accumulator rows of lane quarter g read the
-//      scales of W row n from lane 32g + n % 32, column SFB + 8j + n/32, so
-//      every quarter holds a copy (64 columns per stage).
-constexpr int KSTEPS = 4 * KT;      // K=64 MMA steps per stage
-constexpr uint32_t SF_COL = 256;
-constexpr uint32_t SFA_COLS = 4 * KSTEPS;
-constexpr uint32_t SFB_COLS = 8 * KSTEPS;
-constexpr uint32_t SF_STAGE_COLS = SFA_COLS + SFB_COLS;
+constexpr uint32_t SF_COL = 256;    // per stage and k-tile: 16 columns of A scales, 32 of W scales
+constexpr uint32_t SF_STAGE_COLS = 48 * KT;
 static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
-static_assert(SFA_COLS == 32 && SFB_COLS == 64, "scale stores are written 32 columns at a time");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment for 128B swizzle");
 
@@ -90,16 +79,19 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
          (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
+// Descriptor for tcgen05.cp of a 32-row x 16-byte block: rows 16 bytes
+// apart, 8-row core matrices 128 bytes apart, no swizzle.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(128 >> 4) << 32) | (uint64_t(1) << 46);
+}
 
 struct Smem {
-  uint8_t* stage;      // STAGES x [A | B | SFA | SFB]
-  uint8_t* epi;        // EPI_WARPS x 32 rows x 256 BF16
-  uint64_t* full;      // leader: A and W bytes of both CTAs have landed
-  uint64_t* sf_full;   // each CTA: its own scale bytes have landed
-  uint64_t* sf_ready;  // leader: scales of both CTAs are in tensor memory
-  uint64_t* empty;     // each CTA: the stage may be refilled
-  uint64_t* tfull;     // each CTA: accumulators complete
-  uint64_t* tempty;    // leader: accumulators of both CTAs drained
+  uint8_t* stage;  // STAGES x [A | B | SFA | SFB]
+  uint8_t* epi;    // EPI_WARPS x 32 rows x 256 BF16
+  uint64_t* full;  // used in the leader CTA only
+  uint64_t* empty;
+  uint64_t* tfull;
+  uint64_t* tempty;  // used in the leader CTA only
   uint64_t* mma_done;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -112,13 +104,11 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.epi = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + EPI_BYTES);
   s.full = bars;
-  s.sf_full = bars + STAGES;
-  s.sf_ready = bars + 2 * STAGES;
-  s.empty = bars + 3 * STAGES;
-  s.tfull = bars + 4 * STAGES;
-  s.tempty = bars + 4 * STAGES + 1;
-  s.mma_done = bars + 4 * STAGES + 2;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 3);
+  s.empty = bars + STAGES;
+  s.tfull = bars + 2 * STAGES;
+  s.tempty = bars + 2 * STAGES + 1;
+  s.mma_done = bars + 2 * STAGES + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
 }
@@ -141,14 +131,6 @@ __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag)
   if (p.dev_status != nullptr) atomicExch(p.dev_status, static_cast<uint32_t>(NVFP4_ETIMEOUT));
 }
 
-// One lane of a warp waits; the warp follows its verdict.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p, const volatile int* abort_flag,
-                                          int lane) {
-  int ok = 1;
-  if (lane == 0) ok = mbar_wait_bounded(bar, parity, p.wait_limit_cycles, abort_flag);
-  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
@@ -164,8 +146,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.sf_full[s], 1);
-      mbar_init(&sm.sf_ready[s], 2 * SF_WARPS);
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(sm.tfull, 1);
@@ -198,7 +178,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
         const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
         // Boxes beyond the operands (the last M or N half) are zero-filled by
-        // the TMA and still count their full bytes.
+        // the TMA and still count their full bytes, so every stage carries
+        // 2 x STAGE_BYTES for the leader's barrier.
         const int a_row = mt * PAIR_M + int(rank) * HALF;
         const int b_row = nt * PAIR_N + int(rank) * HALF;
         const int sfa_row0 = (a_row / HALF) * p.sf_panel_rows;
@@ -210,12 +191,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           uint8_t* st = sm.stage + stage * STAGE_BYTES;
           const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * (A_BYTES + B_BYTES));
+          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * STAGE_BYTES);
           tma_load_3d_pair(st, &tmap_a, full_leader, 0, a_row, ks * KT, pol_a);
           tma_load_3d_pair(st + A_BYTES, &tmap_w, full_leader, 0, b_row, ks * KT, pol_w);
-          mbar_arrive_expect_tx(&sm.sf_full[stage], SFA_BYTES + SFB_BYTES);
-          tma_load_2d(st + A_BYTES + B_BYTES, &tmap_sa, &sm.sf_full[stage], 0, sfa_row0 + ks * KT * 8, pol_a);
-          tma_load_3d(st + A_BYTES + B_BYTES + SFA_BYTES, &tmap_sw, &sm.sf_full[stage], 0, ks * KT * 8, nt * 2, pol_w);
+          tma_load_2d_pair(st + A_BYTES + B_BYTES, &tmap_sa, full_leader, 0, sfa_row0 + ks * KT * 8, pol_a);
+          tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmap_sw, full_leader, 0, ks * KT * 8, nt * 2, pol_w);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -237,26 +217,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         for (int ks = 0; ks < p.num_stages_k; ++ks) {
-          if (!mbar_wait_bounded(&sm.full[stage], phase, p.wait_limit_cycles, abort_flag) ||
-              !mbar_wait_bounded(&sm.sf_ready[stage], phase, p.wait_limit_cycles, abort_flag)) {
+          if (!mbar_wait_bounded(&sm.full[stage], phase, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
             break;
           }
           tc_fence_after();
           const uint8_t* st = sm.stage + stage * STAGE_BYTES;
-          const uint32_t sfa_tmem = tmem + SF_COL + stage * SF_STAGE_COLS;
-          const uint32_t sfb_tmem = sfa_tmem + SFA_COLS;
+          const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + A_BYTES);
+          const uint32_t sfa_addr = smem_u32(st + A_BYTES + B_BYTES);
+          const uint32_t sfb_addr = sfa_addr + SFA_BYTES;
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
-            const uint64_t a_desc = desc_sw128(smem_u32(st + kk * KTILE_BYTES));
-            const uint64_t b_desc = desc_sw128(smem_u32(st + A_BYTES + kk * KTILE_BYTES));
+            const uint32_t sfa_tmem = tmem + SF_COL + stage * SF_STAGE_COLS + kk * 48;
+            const uint32_t sfb_tmem = sfa_tmem + 16;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tc_cp_pair_32x128b_warpx4(sfa_tmem + 4 * j, desc_sf(sfa_addr + kk * 2048 + 512 * j));
+              tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j, desc_sf(sfb_addr + kk * 2048 + 512 * j));
+              tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j + 4, desc_sf(sfb_addr + SFB_PANEL + kk * 2048 + 512 * j));
+            }
+            const uint64_t a_desc = desc_sw128(a_addr + kk * KTILE_BYTES), b_desc = desc_sw128(b_addr + kk * KTILE_BYTES);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               // K step j: 64 elements = 32 bytes further along the swizzled row
-              const int step = kk * 4 + j;
-              tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sfa_tmem + 4 * step,
-                               sfb_tmem + 8 * step, (ks | kk | j) != 0);
+              tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sfa_tmem + 4 * j,
+                               sfb_tmem + 8 * j, (ks | kk | j) != 0);
             }
           }
           tc_commit_pair(&sm.empty[stage]);  // frees the stage in both CTAs once these MMAs complete
@@ -272,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // in either CTA when the pair tears down.
       tc_commit_pair(sm.mma_done);
     }
-  } else if (warp < 2 + EPI_WARPS) {
+  } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
@@ -281,7 +267,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
       const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
-      if (!warp_wait(sm.tfull, local & 1, p, abort_flag, lane)) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(sm.tfull, local & 1, p.wait_limit_cycles, abort_flag);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
         if (lane == 0) report_timeout(p, sm.abort_flag);
         break;
       }
@@ -337,66 +326,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
     if (lane == 0) bulk_wait_all();
-  } else {
-    // ------------------------------------------------------------ scale writers (both CTAs)
-    // Move this CTA's scale bytes from the stage (tiled layout: the four
-    // scales of row 32g + r for one K=64 step at byte 16r + 4g of that step's
-    // 512-byte chunk) into the tensor-memory layout the MMA reads.
-    const int q = warp & 3;  // lane quarter: A rows 32q..32q+31 and this quarter's copy of the W scales
-    const uint32_t sf_ready_leader_base = mapa_shared(smem_u32(sm.sf_ready), 0);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-      for (int ks = 0; ks < p.num_stages_k; ++ks) {
-        if (!warp_wait(&sm.sf_full[stage], phase, p, abort_flag, lane)) {
-          if (lane == 0) report_timeout(p, sm.abort_flag);
-          ok = false;
-          break;
-        }
-        const uint8_t* sfa = sm.stage + stage * STAGE_BYTES + A_BYTES + B_BYTES;
-        const uint8_t* sfb = sfa + SFA_BYTES;
-        const uint32_t sfa_tmem = tmem + (uint32_t(q * 32) << 16) + SF_COL + stage * SF_STAGE_COLS;
-        uint32_t v[32];
-#pragma unroll
-        for (int j = 0; j < KSTEPS; ++j) {
-          const uint32_t wj = *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 16 * lane + 4 * q);
-          v[4 * j] = wj;
-          v[4 * j + 1] = wj;
-          v[4 * j + 2] = wj;
-          v[4 * j + 3] = wj;
-        }
-        tmem_st_32x32b_x32(sfa_tmem, v);
-        {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int j = half * 4 + jj;
-              const uint4 p0 = *reinterpret_cast<const uint4*>(sfb + 512 * j + 16 * lane);
-              const uint4 p1 = *reinterpret_cast<const uint4*>(sfb + SFB_PANEL + 512 * j + 16 * lane);
-              v[8 * jj + 0] = p0.x;
-              v[8 * jj + 1] = p0.y;
-              v[8 * jj + 2] = p0.z;
-              v[8 * jj + 3] = p0.w;
-              v[8 * jj + 4] = p1.x;
-              v[8 * jj + 5] = p1.y;
-              v[8 * jj + 6] = p1.z;
-              v[8 * jj + 7] = p1.w;
-            }
-            tmem_st_32x32b_x32(sfa_tmem + SFA_COLS + 32 * half, v);
-          }
-        }
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(sf_ready_leader_base + 8u * uint32_t(stage));
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
   }
 
   // teardown: every MMA of the pair has completed before tensor memory is freed
