@@ -49,7 +49,7 @@ def _headers() -> list[str]:
 
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(GEN, exist_ok=True)
-    table = os.path.join(GEN, "silu_mid_table.inc")
+    table = os.path.join(GEN, "silu_table_full.inc")
     gen = os.path.join(CSRC, "gen_silu_table.py")
     if force or _newer(table, [gen]):
         subprocess.check_call([sys.executable, gen, table])

@@ -16,9 +16,10 @@
 // h is never stored.  The scale finalize is folded into pass 2's prologue,
 // the zeroing into its stores.
 //
-// Work unit: one warp handles 256 consecutive elements of one row; lane l
-// owns elements 8l..8l+7 (one 16-byte load of gate, one of up), a lane pair
-// owns one 16-element block, eight lanes one 4-column group of scales.
+// Work unit: one warp handles 512 consecutive elements of one row; lane l
+// owns the 16-element block 16l..16l+15 (two 16-byte loads of gate, two of
+// up), four lanes one 4-column group of scales.  SwiGLU kernels keep the
+// 65,536-entry BF16 silu table (128 KB) in shared memory, one CTA per SM.
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -28,66 +29,50 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kSiluEntries = 3840;
+// SwiGLU kernels run one CTA of 1024 threads per SM with the whole silu table
+// (128 KB) in shared memory; weight kernels need no table.
+constexpr int kThreadsSwiglu = 1024;
+constexpr int kThreadsWeight = 256;
 constexpr int kSegElems = 512;  // elements of one row handled by one warp per unit (16 per lane)
+constexpr int kTableBytes = 65536 * 2;
 
-// Correctly rounded BF16 silu for gates with exponent field 117..129 (g > 0,
-// entries 0..1663) and 117..133 (g < 0, entries 1664..3839), indexed by
-// (g & 0x7FFF) - 117*128; generated at build time by gen_silu_table.py.
-__device__ const uint16_t k_silu_mid[kSiluEntries] = {
-#include "silu_mid_table.inc"
+// Correctly rounded BF16 silu of every BF16 gate, indexed by its bit pattern;
+// generated at build time by gen_silu_table.py.  Closed forms behind it:
+// |g| < 2^-10 gives g/2 (a lost bit rounds toward +inf: silu(g) > g/2),
+// g >= 8 gives g, g <= -128 gives -0, +inf gives +inf, -inf and NaN give NaN.
+__device__ const uint16_t k_silu_tab[65536] = {
+#include "silu_table_full.inc"
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
-// silu(g) rounded once to BF16, for the gates outside the table:
-//   |g| < 2^-10 : silu(g) = g/2 + g^2/4 - ..., so the result is g/2, and when
-//                 g/2 falls between two BF16 values the exact value lies
-//                 above the midpoint: round toward +inf.
-//   g >= 8      : the relative gap g - silu(g) < e^-8 < 2^-9: the result is g.
-//   g <= -128   : |silu(g)| < 2^-134: the result is -0.
-//   +inf -> +inf, -inf and NaN -> NaN (a non-finite gate stays non-finite).
-__device__ __noinline__ float silu_outside_table(uint32_t g) {
-  const uint32_t mag = g & 0x7FFFu;
-  const uint32_t neg = g >> 15;
-  uint32_t out;
-  if (mag < 117u * 128u) {
-    const uint32_t u = __float_as_uint(bf16_to_f32(g) * 0.5f);  // exact, no flush to zero
-    out = (u + (neg ? 0x7FFFu : 0x8000u)) >> 16;
-  } else if (mag >= 0x7F80u) {
-    out = (g == 0x7F80u) ? 0x7F80u : 0x7FC0u;
-  } else {
-    out = neg ? 0x8000u : g;
-  }
-  return bf16_to_f32(out);
+// silu of both BF16 gates in a word, as a BF16 pair.
+__device__ __forceinline__ uint32_t silu_pair(uint32_t gw, const uint16_t* tab) {
+  return uint32_t(tab[gw & 0xFFFFu]) | (uint32_t(tab[gw >> 16]) << 16);
 }
 
-// silu(g) rounded once to BF16 (returned as its binary32 value); the common
-// case is one shared-memory load from the table (entries stored as binary32).
-__device__ __forceinline__ float silu_bf16(uint32_t g, const float* tab) {
-  const uint32_t rel = (g & 0x7FFFu) - 117u * 128u;
-  const bool neg = (g & 0x8000u) != 0;
-  if (rel < (neg ? 2176u : 1664u)) return tab[rel + (neg ? 1664u : 0u)];
-  return silu_outside_table(g);
+// Two SwiGLU outputs h = RNE_bf16(silu_bf16(g) * u): the BF16 product of two
+// BF16 values is their exact binary32 product rounded once (mul.rn.bf16x2).
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw, const uint16_t* tab) {
+  const uint32_t sw = silu_pair(gw, tab);
+  const __nv_bfloat162 h = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&sw),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&uw));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// The exact binary32 product silu_bf16(g) * u (two BF16 significands: no
-// rounding); h = RNE_bf16 of it.
-__device__ __forceinline__ float swiglu_product(uint32_t g, uint32_t u, const float* tab) {
-  return __fmul_rn(silu_bf16(g, tab), bf16_to_f32(u));
-}
-
-// Two SwiGLU outputs as BF16 bits (lo in bits 0..15).
-__device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw, const float* tab) {
-  return bf16x2_rn(swiglu_product(gw & 0xFFFFu, uw & 0xFFFFu, tab), swiglu_product(gw >> 16, uw >> 16, tab));
+// Elementwise max of two BF16 pairs (NaN propagates).
+__device__ __forceinline__ uint32_t max_pair(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 m = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&m);
 }
 
 template <bool kSwiglu>
-__device__ __forceinline__ void load_table(float* tab) {
+__device__ __forceinline__ void load_table(uint16_t* tab) {
   if constexpr (kSwiglu) {
-    for (int i = threadIdx.x; i < kSiluEntries; i += blockDim.x) tab[i] = bf16_to_f32(k_silu_mid[i]);
+    const uint4* src = reinterpret_cast<const uint4*>(k_silu_tab);
+    uint4* dst = reinterpret_cast<uint4*>(tab);
+    for (int i = threadIdx.x; i < kTableBytes / 16; i += blockDim.x) dst[i] = src[i];
     __syncthreads();
   }
 }
@@ -95,62 +80,65 @@ __device__ __forceinline__ void load_table(float* tab) {
 // Raw 16-element slice of one lane: 2 x 16 B of gate (or W) and, with
 // SwiGLU, 2 x 16 B of up.
 struct Slice {
-  uint4 g[2];
-  uint4 u[2];
+  uint32_t g[8];
+  uint32_t u[8];
 };
 
 template <bool kSwiglu, bool kStream>
 __device__ __forceinline__ void load_slice(const uint16_t* row, int64_t cols, int64_t c0, Slice& s) {
   const uint4* pg = reinterpret_cast<const uint4*>(row + c0);
+  uint4 a, b;
   if constexpr (kStream) {
-    s.g[0] = __ldcs(pg);
-    s.g[1] = __ldcs(pg + 1);
+    a = __ldcs(pg);
+    b = __ldcs(pg + 1);
   } else {
-    s.g[0] = __ldg(pg);
-    s.g[1] = __ldg(pg + 1);
+    a = __ldg(pg);
+    b = __ldg(pg + 1);
   }
+  s.g[0] = a.x, s.g[1] = a.y, s.g[2] = a.z, s.g[3] = a.w, s.g[4] = b.x, s.g[5] = b.y, s.g[6] = b.z, s.g[7] = b.w;
   if constexpr (kSwiglu) {
     const uint4* pu = reinterpret_cast<const uint4*>(row + cols + c0);
     if constexpr (kStream) {
-      s.u[0] = __ldcs(pu);
-      s.u[1] = __ldcs(pu + 1);
+      a = __ldcs(pu);
+      b = __ldcs(pu + 1);
     } else {
-      s.u[0] = __ldg(pu);
-      s.u[1] = __ldg(pu + 1);
+      a = __ldg(pu);
+      b = __ldg(pu + 1);
     }
+    s.u[0] = a.x, s.u[1] = a.y, s.u[2] = a.z, s.u[3] = a.w, s.u[4] = b.x, s.u[5] = b.y, s.u[6] = b.z, s.u[7] = b.w;
   }
 }
 
-__device__ __forceinline__ uint32_t word(const Slice& s, int i, bool up) {
-  const uint4& v = up ? s.u[i >> 2] : s.g[i >> 2];
-  return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
-}
-
-// max |h| of a slice as a binary32 bit pattern.  With SwiGLU the exact
-// products are compared and the largest is rounded to BF16 once: rounding is
-// monotone, so max |RNE(p)| = RNE(max |p|).  Integer max keeps NaN (its bit
+// max |h| of a slice as a binary32 bit pattern (integer max keeps NaN: its bit
 // patterns sort above +inf).
 template <bool kSwiglu>
-__device__ __forceinline__ uint32_t slice_absmax_bits(const Slice& s, const float* tab) {
+__device__ __forceinline__ uint32_t slice_absmax_bits(const Slice& s, const uint16_t* tab) {
   uint32_t m = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t gw = word(s, i, false);
-    if constexpr (kSwiglu) {
-      const uint32_t uw = word(s, i, true);
-      m = max(m, __float_as_uint(swiglu_product(gw & 0xFFFFu, uw & 0xFFFFu, tab)) & 0x7FFFFFFFu);
-      m = max(m, __float_as_uint(swiglu_product(gw >> 16, uw >> 16, tab)) & 0x7FFFFFFFu);
-    } else {
-      m = max(m, (gw << 16) & 0x7FFFFFFFu);
-      m = max(m, gw & 0x7FFF0000u);
-    }
+    const uint32_t hw = kSwiglu ? swiglu_pair(s.g[i], s.u[i], tab) : s.g[i];
+    m = max(m, max((hw << 16) & 0x7FFFFFFFu, hw & 0x7FFF0000u));
   }
   return m;
 }
 
-__device__ __forceinline__ uint32_t round_max_to_bf16(uint32_t m) {
-  if (m >= 0x7F800000u) return m;  // Inf / NaN stay as they are
-  return bf16x2_rn(__uint_as_float(m), 0.0f) << 16;
+// An upper bound of max |h| over a SwiGLU slice, exact to apply: |silu(g)|
+// is at most max(g, 0.2785) for every g, hence at most max(|g|, 0.28125),
+// so |h| = RNE(|silu_bf16(g) u|) <= RNE(max(|g|, 0.28125) |u|), which is
+// what mul.rn.bf16x2 returns.  NaN and Inf inputs give a NaN or Inf bound.
+__device__ __forceinline__ float slice_bound(const Slice& s) {
+  const uint32_t c = 0x3E903E90u;  // 0.28125 in both halves
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t ga = max_pair(s.g[i] & 0x7FFF7FFFu, c);
+    const uint32_t ua = s.u[i] & 0x7FFF7FFFu;
+    const __nv_bfloat162 b = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&ga),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&ua));
+    m = max_pair(m, *reinterpret_cast<const uint32_t*>(&b));
+  }
+  // the larger half, by bit pattern so that a NaN half wins
+  return __uint_as_float(max((m << 16) & 0x7FFFFFFFu, m & 0x7FFF0000u));
 }
 
 // Walks the units (row, segment) of a [rows, cols] grid, grid-strided over
@@ -175,20 +163,21 @@ struct UnitWalker {
 };
 
 // Pass 1: rec->amax_bits = max over the tensor of the bit pattern of |h|.
-// Two units in flight per warp.  Loads keep the default L2 policy so the
-// tail of the tensor is still in L2 when pass 2 (which walks backwards)
-// starts.
+// Each lane keeps the exact max of what it has evaluated; a SwiGLU slice whose
+// bound does not exceed that max cannot change it and is skipped.  Two units
+// in flight per warp; loads keep the default L2 policy so the tail of the
+// tensor is still in L2 when pass 2 (which walks backwards) starts.
 template <bool kSwiglu>
-__global__ void __launch_bounds__(kThreads) k_amax(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                                                   int64_t ld, nvfp4_scale_rec* rec) {
-  __shared__ float tab[kSwiglu ? kSiluEntries : 1];
-  __shared__ uint32_t wmax[kWarps];
+__global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
+    k_amax(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, nvfp4_scale_rec* rec) {
+  extern __shared__ __align__(16) uint16_t tab[];
+  __shared__ uint32_t wmax[32];
   load_table<kSwiglu>(tab);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int64_t segs = (cols + kSegElems - 1) / kSegElems;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
-  uint32_t amax = 0;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
+  uint32_t amax = 0;  // bit pattern of the exact max |h| this lane has evaluated
   UnitWalker w(first, stride, segs);
   while (w.row < rows) {
     const int64_t r0 = w.row, c0 = w.seg * kSegElems + lane * 16;
@@ -199,17 +188,21 @@ __global__ void __launch_bounds__(kThreads) k_amax(const uint16_t* __restrict__ 
     const bool v0 = c0 < cols, v1 = r1 < rows && c1 < cols;
     if (v0) load_slice<kSwiglu, false>(x + r0 * ld, cols, c0, s0);
     if (v1) load_slice<kSwiglu, false>(x + r1 * ld, cols, c1, s1);
-    if (v0) amax = max(amax, slice_absmax_bits<kSwiglu>(s0, tab));
-    if (v1) amax = max(amax, slice_absmax_bits<kSwiglu>(s1, tab));
+    if constexpr (kSwiglu) {
+      // exact evaluation only where the bound could beat the running max
+      if (v0 && !(slice_bound(s0) <= __uint_as_float(amax))) amax = max(amax, slice_absmax_bits<true>(s0, tab));
+      if (v1 && !(slice_bound(s1) <= __uint_as_float(amax))) amax = max(amax, slice_absmax_bits<true>(s1, tab));
+    } else {
+      if (v0) amax = max(amax, slice_absmax_bits<false>(s0, tab));
+      if (v1) amax = max(amax, slice_absmax_bits<false>(s1, tab));
+    }
   }
   amax = __reduce_max_sync(0xFFFFFFFFu, amax);
   if (lane == 0) wmax[warp] = amax;
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < kWarps; ++i) m = max(m, wmax[i]);
-    if constexpr (kSwiglu) m = round_max_to_bf16(m);
+    for (int i = 0; i < nwarps; ++i) m = max(m, wmax[i]);
     if (m != 0) atomicMax(&rec->amax_bits, m);
   }
 }
@@ -232,16 +225,18 @@ __device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float 
   return e4m3_code(r);
 }
 
-// Pass 2: quantise.  Units cover rows [0, rows_pad), walked from the end so
-// that the first reads hit what pass 1 left in L2; rows >= rows are zeros.
+// Pass 2: quantise.  One lane = one 16-element block.  Units cover rows
+// [0, rows_pad), walked from the end so that the first reads hit what pass 1
+// left in L2; rows >= rows are zeros.
 template <bool kSwiglu>
-__global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                                                    int64_t ld, int64_t rows_pad, uint8_t* __restrict__ qdata,
-                                                    uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
-  __shared__ float tab[kSwiglu ? kSiluEntries : 1];
+__global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
+    k_quant(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int64_t rows_pad,
+            uint8_t* __restrict__ qdata, uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
+  extern __shared__ __align__(16) uint16_t tab[];
   load_table<kSwiglu>(tab);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
+  // Global scale from pass 1's record (the bit pattern of max |h|).
   const uint32_t amax_bits = *reinterpret_cast<volatile uint32_t*>(&rec->amax_bits);
   const bool finite = amax_bits < 0x7F800000u;
   const float g = finite ? __fdiv_rn(__uint_as_float(amax_bits), 2688.0f) : __uint_as_float(0x7FC00000u);
@@ -254,8 +249,8 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__
 
   const int64_t segs = (cols + kSegElems - 1) / kSegElems;
   const int64_t cpad4 = (cols / 16 + 3) / 4;  // 4-column scale groups per row
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
   for (UnitWalker w(first, stride, segs); w.row < rows_pad; w.next()) {
     const int64_t r = rows_pad - 1 - w.row;
     const int64_t seg = segs - 1 - w.seg;
@@ -266,16 +261,16 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__
       Slice s;
       load_slice<kSwiglu, true>(x + r * ld, cols, c0, s);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(word(s, i, false), word(s, i, true), tab)
-                                                  : word(s, i, false);
+      for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(s.g[i], s.u[i], tab) : s.g[i];
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) hw[i] = 0u;
     }
-    uint32_t mbits = 0;
+    uint32_t m2 = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mbits = max(mbits, max((hw[i] << 16) & 0x7FFFFFFFu, hw[i] & 0x7FFF0000u));
-    const uint32_t bs = finite ? block_scale_code(__uint_as_float(mbits), d, rd) : 0u;
+    for (int i = 0; i < 8; ++i) m2 = max_pair(m2, hw[i] & 0x7FFF7FFFu);
+    const float bmax = __uint_as_float(max((m2 << 16) & 0x7FFFFFFFu, m2 & 0x7FFF0000u));
+    const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
     const float sc = __fmul_rn(e4m3_value(bs), g);
     uint2 packed = make_uint2(0u, 0u);
     if (sc != 0.0f && finite) {
@@ -316,11 +311,16 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__
 }
 
 template <typename K>
-int grid_for(K kernel) {
+nvfp4_status launch_stream_kernel(K kernel, bool swiglu, cudaStream_t stream, const char* name, auto... args) {
+  const int threads = swiglu ? kThreadsSwiglu : kThreadsWeight;
+  const int smem = swiglu ? kTableBytes : 0;
+  nvfp4_status st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem), name);
+  if (st != NVFP4_OK) return st;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
-  return sm_count() * per_sm;
+  kernel<<<sm_count() * per_sm, threads, smem, stream>>>(args...);
+  return cuda_check(cudaGetLastError(), name);
 }
 
 nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, bool swiglu, void* qdata,
@@ -342,41 +342,49 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
   nvfp4_status st = cuda_check(cudaMemsetAsync(rec, 0, sizeof(nvfp4_scale_rec), stream), "memset rec");
   if (st != NVFP4_OK) return st;
   if (swiglu) {
-    k_amax<true><<<grid_for(k_amax<true>), kThreads, 0, stream>>>(xin, rows, cols, ld, rec);
-    st = cuda_check(cudaGetLastError(), "launch k_amax");
-    if (st != NVFP4_OK) return st;
-    k_quant<true><<<grid_for(k_quant<true>), kThreads, 0, stream>>>(xin, rows, cols, ld, rows_pad, q, s, rec);
-  } else {
-    k_amax<false><<<grid_for(k_amax<false>), kThreads, 0, stream>>>(xin, rows, cols, ld, rec);
-    st = cuda_check(cudaGetLastError(), "launch k_amax");
-    if (st != NVFP4_OK) return st;
-    k_quant<false><<<grid_for(k_quant<false>), kThreads, 0, stream>>>(xin, rows, cols, ld, rows_pad, q, s, rec);
+    if ((st = launch_stream_kernel(k_amax<true>, true, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
+      return st;
+    return launch_stream_kernel(k_quant<true>, true, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
   }
-  return cuda_check(cudaGetLastError(), "launch k_quant");
+  if ((st = launch_stream_kernel(k_amax<false>, false, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
+    return st;
+  return launch_stream_kernel(k_quant<false>, false, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
 }
 
 // ---- diagnostics: the same device functions on test-chosen inputs ----------
 
 __global__ void k_diag_silu_all(uint16_t* out) {
-  __shared__ float tab[kSiluEntries];
+  extern __shared__ __align__(16) uint16_t tab[];
   load_table<true>(tab);
   for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < 65536u; g += gridDim.x * blockDim.x)
-    out[g] = static_cast<uint16_t>(__float_as_uint(silu_bf16(g, tab)) >> 16);
+    out[g] = static_cast<uint16_t>(silu_pair(g, tab) & 0xFFFFu);
 }
 
-// SwiGLU through the producer's pass-2 path (swiglu_pair) and, for the
-// pass-1 path, the BF16 rounding of the exact product.
+// SwiGLU through the producer's pass-2 path (swiglu_pair, both halves of the
+// word), checked against pass 1's path (exact product, rounded once at the
+// end) and pass 1's bound; a disagreement is reported as the NaN pattern
+// 0x7FFF, which never equals the oracle.
 __global__ void k_diag_swiglu(const uint16_t* gate, const uint16_t* up, uint16_t* h, int64_t n) {
-  __shared__ float tab[kSiluEntries];
+  extern __shared__ __align__(16) uint16_t tab[];
   load_table<true>(tab);
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint32_t pair = swiglu_pair(gate[i] | (uint32_t(gate[i]) << 16), up[i] | (uint32_t(up[i]) << 16), tab);
-    const uint32_t p1 = round_max_to_bf16(__float_as_uint(swiglu_product(gate[i], up[i], tab)) & 0x7FFFFFFFu) >> 16;
+    const uint32_t gw = gate[i] | (uint32_t(gate[i]) << 16), uw = up[i] | (uint32_t(up[i]) << 16);
+    const uint32_t pair = swiglu_pair(gw, uw, tab);
+    const float p = __fmul_rn(bf16_to_f32(tab[gate[i]]), bf16_to_f32(up[i]));
+    const uint32_t pa = __float_as_uint(p) & 0x7FFFFFFFu;
+    const uint32_t p1 = (pa >= 0x7F800000u ? pa : (bf16x2_rn(__uint_as_float(pa), 0.0f) << 16)) >> 16;
+    Slice s;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      s.g[k] = gw;
+      s.u[k] = uw;
+    }
+    const float bound = slice_bound(s);
     const uint32_t lo = pair & 0xFFFFu, hi = pair >> 16;
-    // both halves of the pair and |pass-1 value| must agree; a disagreement
-    // is reported as the NaN pattern 0x7FFF, which never equals the oracle
-    const bool ok = lo == hi && ((lo & 0x7FFFu) == p1 || ((lo & 0x7FFFu) > 0x7F80u && p1 > 0x7F80u));
+    const bool nan_h = (lo & 0x7FFFu) > 0x7F80u;
+    const bool bound_ok = nan_h || isnan(bound) || bf16_to_f32(lo & 0x7FFFu) <= bound;
+    const bool ok = lo == hi && ((lo & 0x7FFFu) == p1 || (nan_h && p1 > 0x7F80u)) && bound_ok;
     h[i] = static_cast<uint16_t>(ok ? lo : 0x7FFFu);
   }
 }
@@ -437,14 +445,20 @@ extern "C" nvfp4_status swiglu_nvfp4_quantize(const void* gate_up_bf16, int64_t 
 
 extern "C" nvfp4_status nvfp4_diag_silu_all(uint16_t* out, nvfp4_stream_t stream) {
   if (!out || !aligned16(out)) return fail(NVFP4_EINVAL, "nvfp4_diag_silu_all: bad pointer");
-  k_diag_silu_all<<<64, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(out);
+  nvfp4_status st = cuda_check(
+      cudaFuncSetAttribute(k_diag_silu_all, cudaFuncAttributeMaxDynamicSharedMemorySize, kTableBytes), "diag silu");
+  if (st != NVFP4_OK) return st;
+  k_diag_silu_all<<<64, 256, kTableBytes, reinterpret_cast<cudaStream_t>(stream)>>>(out);
   return cuda_check(cudaGetLastError(), "launch k_diag_silu_all");
 }
 
 extern "C" nvfp4_status nvfp4_diag_swiglu(const uint16_t* gate, const uint16_t* up, uint16_t* h, int64_t n,
                                           nvfp4_stream_t stream) {
   if (!gate || !up || !h || n < 1) return fail(NVFP4_EINVAL, "nvfp4_diag_swiglu: bad arguments");
-  k_diag_swiglu<<<256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(gate, up, h, n);
+  nvfp4_status st = cuda_check(
+      cudaFuncSetAttribute(k_diag_swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize, kTableBytes), "diag swiglu");
+  if (st != NVFP4_OK) return st;
+  k_diag_swiglu<<<64, 256, kTableBytes, reinterpret_cast<cudaStream_t>(stream)>>>(gate, up, h, n);
   return cuda_check(cudaGetLastError(), "launch k_diag_swiglu");
 }
 
