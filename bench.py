@@ -55,6 +55,22 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank time over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flop_per_step: float, step_seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank runs a replica, time is the slowest rank's."""
+    return world * flop_per_step / step_seconds / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -289,13 +305,9 @@ def run_ours(args):
     if int(status.item()) != 0:
         raise RuntimeError("GEMM reported a device timeout")
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * FLOP / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(world, FLOP, ms_per_step * 1e-3)
 
     # ---- end to end through the public host-buffer call
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
@@ -310,12 +322,8 @@ def run_ours(args):
         fc2.nvfp4_quantize_weight(w, wq, stream)
         fc2.fc2_host(x_host, wq, ws, stream, out_host)
     e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * FLOP / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+    e2e_s = max_over_ranks(e2e_s, dev)
+    e2e = {"value": job_throughput(world, FLOP, e2e_s), "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2,
            "steps": e2e_steps, "api": "nvfp4_quantize_weight + fc2_host (pinned host gate|up in, host BF16 out)"}
 
