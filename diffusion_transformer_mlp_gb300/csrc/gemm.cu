@@ -7,22 +7,33 @@
 // and the activation about 42x; the winning schedule keeps those re-reads
 // in L2; no global atomics, no reduction traffic, one output write).
 // The pages' kernel is a GB10 warp-MMA library kernel; this one is written
-// for the datacenter Blackwell tensor core instead:
+// for the datacenter Blackwell tensor core instead.  A CTA pair computes a
+// 256 x 256 output tile with tcgen05.mma.cta_group::2 (M=256, N=256, K=64
+// per instruction); each CTA holds 128 rows of A and 128 rows of W per
+// k-tile and a 128 x 256 FP32 accumulator in its tensor memory.
 //
-//   warp 0      TMA producer: per k-tile (256 K elements) one 128x128-byte
-//               A tile and one W tile (128B swizzle) plus the two 2 KB
-//               block-scale chunks (already in the tiled layout the tensor
-//               core reads), into a STAGES-deep shared-memory ring.
-//   warp 1      MMA issuer: tcgen05.cp of the scale chunks into tensor
-//               memory, four tcgen05.mma kind::mxf4nvf4 (K=64 each) per
-//               k-tile into a 128x128 FP32 accumulator in tensor memory;
-//               two accumulators so the epilogue of tile i overlaps the
-//               main loop of tile i+1.
-//   warps 2-5   epilogue: tcgen05.ld, multiply by alpha = gA*gW, round to
-//               BF16, stage through 128B-swizzled shared memory, TMA store
-//               (clipped at row M).
+//   warp 0      TMA producer (both CTAs): per stage KT k-tiles (256 K
+//               elements each) of this CTA's 128 A rows and 128 W rows
+//               (128B swizzle) into a STAGES-deep shared-memory ring; the
+//               leader's barrier counts both CTAs' bytes.
+//   warp 1      MMA issuer (leader CTA): per stage one wait, 4*KT MMAs
+//               reading the operands from the stage and the block scales
+//               from the stage's tensor-memory slot, one commit; nothing
+//               else goes through the tensor pipe.
+//   warps 2-5   epilogue (both CTAs): tcgen05.ld, multiply by
+//               alpha = gA*gW, round to BF16, stage through 128B-swizzled
+//               shared memory, TMA store (clipped at row M).
+//   warps 6-9   scale writers (both CTAs), one per TMEM lane quarter: read
+//               a stage's UE4M3 words straight from the tiled scale layout
+//               in global memory (one stage ahead, in registers), store them
+//               with tcgen05.st into the stage's tensor-memory slot in the
+//               layout the MMA reads, and arrive on the leader's stage
+//               barrier next to the TMA bytes.  A tcgen05.cp of the scales
+//               would sit in the tensor pipe between the MMAs (a 32x128b
+//               warpx4 copy costs about half an MMA there); tcgen05.st from
+//               other warps does not.
 //
-// Tiles are walked M-panel-major (all N tiles of one 128-row panel, then
+// Tiles are walked M-panel-major (all N tiles of one 256-row panel, then
 // the next), so the CTAs running at any moment share a few activation
 // panels and the whole 43 MB weight through L2.  K is reduced in increasing
 // order inside one CTA: no split-K, no workspace, no atomics, and an output
@@ -37,9 +48,6 @@
 namespace nvfp4 {
 namespace {
 
-// Tile of one CTA pair: 256 rows of A x 256 rows of W (256 x 256 outputs);
-// each CTA holds 128 rows of A and 128 rows of W per stage and 128 x 256
-// FP32 accumulators in its tensor memory.
 constexpr int PAIR_M = 256;
 constexpr int PAIR_N = 256;
 constexpr int HALF = 128;
@@ -49,20 +57,31 @@ constexpr int STAGES = 2;
 constexpr int KTILE_BYTES = HALF * BK_BYTES;   // 16 KB: 128 rows x one k-tile
 constexpr int A_BYTES = KT * KTILE_BYTES;      // this CTA's 128 A rows x KT k-tiles
 constexpr int B_BYTES = KT * KTILE_BYTES;      // this CTA's 128 W rows x KT k-tiles
-constexpr int SFA_BYTES = KT * 2048;           // this CTA's 128 rows x 16 scales per k-tile
-constexpr int SFB_PANEL = KT * 2048;           // one 128-row W panel
-constexpr int SFB_BYTES = 2 * SFB_PANEL;       // all 256 W rows of the tile
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 76 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 4;
+constexpr int SF_WARPS = 4;
+constexpr int WARP_EPI0 = 2;
+constexpr int WARP_SF0 = WARP_EPI0 + EPI_WARPS;
 constexpr int EPI_BYTES = HALF * PAIR_N * 2;   // 128 rows x 256 BF16
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int THREADS = (WARP_SF0 + SF_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;     // 256 FP32 columns
-constexpr uint32_t SF_COL = 256;    // per stage and k-tile: 16 columns of A scales, 32 of W scales
-constexpr uint32_t SF_STAGE_COLS = 48 * KT;
-static_assert(SF_COL + STAGES * SF_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
+constexpr uint32_t ACC_COL = 0;  // 256 FP32 columns
+// Block scales in tensor memory, one slot per operand stage (4*KT K=64
+// steps j):
+//   A: step j at column slot + 4j; the scales of accumulator row i are read
+//      from lane i, column slot + 4j + i/32 (the word is stored in all four
+//      columns).
+//   W: step j at column slot + SFW_COL + 8j; accumulator rows of lane
+//      quarter g read the scales of W row n from lane 32g + n % 32, column
+//      slot + SFW_COL + 8j + n/32, so every quarter holds a copy.
+constexpr int KSTEPS = 4 * KT;  // K=64 steps per stage
+constexpr uint32_t SF_COL = 256;
+constexpr uint32_t SFW_COL = 4 * KSTEPS;
+constexpr uint32_t SF_SLOT_COLS = 12 * KSTEPS;
+static_assert(SF_COL + STAGES * SF_SLOT_COLS <= TMEM_COLS, "tensor memory budget");
+static_assert(KSTEPS == 8, "scale stores are written 32 columns at a time");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment for 128B swizzle");
 
@@ -79,19 +98,15 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
          (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
-// Descriptor for tcgen05.cp of a 32-row x 16-byte block: rows 16 bytes
-// apart, 8-row core matrices 128 bytes apart, no swizzle.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(128 >> 4) << 32) | (uint64_t(1) << 46);
-}
 
 struct Smem {
-  uint8_t* stage;  // STAGES x [A | B | SFA | SFB]
-  uint8_t* epi;    // EPI_WARPS x 32 rows x 256 BF16
-  uint64_t* full;  // used in the leader CTA only
-  uint64_t* empty;
-  uint64_t* tfull;
-  uint64_t* tempty;  // used in the leader CTA only
+  uint8_t* stage;       // STAGES x [A | B]
+  uint8_t* epi;         // EPI_WARPS x 32 rows x 256 BF16
+  uint64_t* full;       // leader: the operand bytes of both CTAs have landed and
+                        // the stage's scales are in both CTAs' tensor memory
+  uint64_t* empty;      // each CTA: the stage (operands and scale slot) may be refilled
+  uint64_t* tfull;      // each CTA: accumulators complete
+  uint64_t* tempty;     // leader: accumulators of both CTAs drained
   uint64_t* mma_done;
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -104,24 +119,27 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.epi = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + EPI_BYTES);
   s.full = bars;
-  s.empty = bars + STAGES;
-  s.tfull = bars + 2 * STAGES;
-  s.tempty = bars + 2 * STAGES + 1;
-  s.mma_done = bars + 2 * STAGES + 2;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
+  s.empty = s.full + STAGES;
+  s.tfull = s.empty + STAGES;
+  s.tempty = s.tfull + 1;
+  s.mma_done = s.tempty + 1;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
 }
+static_assert((2 * STAGES + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
 
 struct Params {
   const nvfp4_scale_rec* a_rec;
   const nvfp4_scale_rec* w_rec;
-  int a_rows;       // padded rows of the activation (multiple of 128)
-  int n;            // weight rows (multiple of 128)
-  int num_m_tiles;  // ceil(a_rows / 256)
-  int num_n_tiles;  // ceil(n / 256)
-  int num_stages_k; // ceil(k / 256 / KT)
-  int sf_panel_rows;  // rows of 256 B per 128-row scale panel: k / 32
+  const uint8_t* a_sf;  // activation block scales, tiled layout
+  const uint8_t* w_sf;  // weight block scales, tiled layout
+  int a_rows;           // padded rows of the activation (multiple of 128)
+  int n;                // weight rows (multiple of 128)
+  int num_m_tiles;      // ceil(a_rows / 256)
+  int num_n_tiles;      // ceil(n / 256)
+  int num_k_tiles;      // k / 256
+  int sf_blocks;        // 512-byte scale blocks per 128-row panel: k / 64
   uint32_t* dev_status;
   uint64_t wait_limit_cycles;
 };
@@ -131,9 +149,98 @@ __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag)
   if (p.dev_status != nullptr) atomicExch(p.dev_status, static_cast<uint32_t>(NVFP4_ETIMEOUT));
 }
 
+// One lane of a warp waits; the warp follows its verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
+                                          const volatile int* abort_flag, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, p.wait_limit_cycles, abort_flag);
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// Position in a ring of `slots` buffers: the slot and the parity of its
+// current use.
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int slots) {
+    if (++slot == slots) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// The scale words one writer lane needs for one stage (K=64 steps
+// j = 0..KSTEPS-1): lane l of quarter q holds A row 32q + l of this CTA's
+// half (one 32-bit word = four scales per step) and W rows 32c + l of the
+// pair's tile, c = 0..7 (one 16-byte line of the tiled layout per 128-row
+// panel and step).
+struct ScaleRegs {
+  uint32_t a[KSTEPS];
+  uint4 w[2 * KSTEPS];  // [2j + panel]
+};
+
+__device__ __forceinline__ uint32_t ldg_nc_u32(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ldg_nc_u128(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// Tiled layout: block (panel, 4-scale column group) of 512 bytes at
+// (panel * sf_blocks + group) * 512; inside it row r of the panel and
+// scale c%4 at (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.  Stage ks,
+// step j is group ks * KSTEPS + j.  Panels past the operand (the second
+// half of a ragged last tile) and steps past K (the second k-tile of a
+// last stage when K / 256 is odd) read as zero scales; the former are
+// never stored, the latter never multiplied.
+__device__ __forceinline__ void load_scales(ScaleRegs& s, const Params& p, int mt, int nt, int ks, uint32_t rank,
+                                            int q, int lane) {
+  const int a_panel = mt * 2 + int(rank);
+  const int w_panel = nt * 2;
+  const int g0 = ks * KSTEPS;
+  const bool a_ok = a_panel * HALF < p.a_rows;
+  const uint8_t* abase = p.a_sf + (size_t(a_panel) * p.sf_blocks + g0) * 512 + lane * 16 + q * 4;
+#pragma unroll
+  for (int j = 0; j < KSTEPS; ++j) s.a[j] = (a_ok && g0 + j < p.sf_blocks) ? ldg_nc_u32(abase + j * 512) : 0u;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const bool w_ok = (w_panel + h) * HALF < p.n;
+    const uint8_t* wbase = p.w_sf + (size_t(w_panel + h) * p.sf_blocks + g0) * 512 + lane * 16;
+#pragma unroll
+    for (int j = 0; j < KSTEPS; ++j)
+      s.w[2 * j + h] = (w_ok && g0 + j < p.sf_blocks) ? ldg_nc_u128(wbase + j * 512) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__device__ __forceinline__ void store_scales(uint32_t taddr, const ScaleRegs& s) {
+  uint32_t va[32], vw[32];
+#pragma unroll
+  for (int j = 0; j < KSTEPS; ++j) va[4 * j] = va[4 * j + 1] = va[4 * j + 2] = va[4 * j + 3] = s.a[j];
+  tmem_st_32x32b_x32(taddr, va);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int jj = 0; jj < KSTEPS / 2; ++jj) {
+      const int j = half * (KSTEPS / 2) + jj;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        vw[8 * jj + 4 * h + 0] = s.w[2 * j + h].x;
+        vw[8 * jj + 4 * h + 1] = s.w[2 * j + h].y;
+        vw[8 * jj + 4 * h + 2] = s.w[2 * j + h].z;
+        vw[8 * jj + 4 * h + 3] = s.w[2 * j + h].w;
+      }
+    }
+    tmem_st_32x32b_x32(taddr + SFW_COL + 32 * half, vw);
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
-               const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
                const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
@@ -142,10 +249,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   const volatile int* abort_flag = sm.abort_flag;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int nk = p.num_k_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sm.full[s], 1);
+      // the producer's expect_tx arrival plus one per scale writer of either CTA
+      mbar_init(&sm.full[s], 1 + 2 * SF_WARPS);
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(sm.tfull, 1);
@@ -155,8 +265,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_w);
-    prefetch_tmap(&tmap_sa);
-    prefetch_tmap(&tmap_sw);
     prefetch_tmap(&tmap_out);
   }
   if (warp == 1) tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
@@ -165,49 +273,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated in both
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer (both CTAs)
+    // ------------------------------------------------------------ operand producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_last();
       const uint64_t pol_a = l2_policy_evict_normal();
-      int stage = 0;
-      uint32_t phase = 0;
+      const int stages_per_tile = (nk + KT - 1) / KT;
+      Ring r;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
-        // Boxes beyond the operands (the last M or N half) are zero-filled by
-        // the TMA and still count their full bytes, so every stage carries
-        // 2 x STAGE_BYTES for the leader's barrier.
+        const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
+        // Boxes beyond the operands (the last M or N half, a k-tile past K)
+        // are zero-filled by the TMA and still count their full bytes, so
+        // every stage carries 2 x STAGE_BYTES for the leader's barrier.
         const int a_row = mt * PAIR_M + int(rank) * HALF;
         const int b_row = nt * PAIR_N + int(rank) * HALF;
-        const int sfa_row0 = (a_row / HALF) * p.sf_panel_rows;
-        for (int ks = 0; ks < p.num_stages_k; ++ks) {
-          if (!mbar_wait_bounded(&sm.empty[stage], phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
+        for (int ks = 0; ks < stages_per_tile; ++ks, r.next(STAGES)) {
+          if (!mbar_wait_bounded(&sm.empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
             break;
           }
-          uint8_t* st = sm.stage + stage * STAGE_BYTES;
-          const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * STAGE_BYTES);
+          uint8_t* st = sm.stage + r.slot * STAGE_BYTES;
+          const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[r.slot]), 0);
+          if (leader) mbar_arrive_expect_tx(&sm.full[r.slot], 2 * STAGE_BYTES);
           tma_load_3d_pair(st, &tmap_a, full_leader, 0, a_row, ks * KT, pol_a);
           tma_load_3d_pair(st + A_BYTES, &tmap_w, full_leader, 0, b_row, ks * KT, pol_w);
-          tma_load_2d_pair(st + A_BYTES + B_BYTES, &tmap_sa, full_leader, 0, sfa_row0 + ks * KT * 8, pol_a);
-          tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmap_sw, full_leader, 0, ks * KT * 8, nt * 2, pol_w);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      int stage = 0;
-      uint32_t phase = 0;
+      const int stages_per_tile = (nk + KT - 1) / KT;
+      Ring ab;
       int local = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs, ++local) {
@@ -216,40 +316,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < p.num_stages_k; ++ks) {
-          if (!mbar_wait_bounded(&sm.full[stage], phase, p.wait_limit_cycles, abort_flag)) {
+        for (int ks = 0; ks < stages_per_tile; ++ks, ab.next(STAGES)) {
+          if (!mbar_wait_bounded(&sm.full[ab.slot], ab.phase, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint8_t* st = sm.stage + stage * STAGE_BYTES;
-          const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + A_BYTES);
-          const uint32_t sfa_addr = smem_u32(st + A_BYTES + B_BYTES);
-          const uint32_t sfb_addr = sfa_addr + SFA_BYTES;
+          const uint32_t st = smem_u32(sm.stage + ab.slot * STAGE_BYTES);
+          const uint32_t sf_tmem = tmem + SF_COL + uint32_t(ab.slot) * SF_SLOT_COLS;
+          const int kk_end = (ks * KT + KT <= nk) ? KT : nk - ks * KT;
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
-            const uint32_t sfa_tmem = tmem + SF_COL + stage * SF_STAGE_COLS + kk * 48;
-            const uint32_t sfb_tmem = sfa_tmem + 16;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_cp_pair_32x128b_warpx4(sfa_tmem + 4 * j, desc_sf(sfa_addr + kk * 2048 + 512 * j));
-              tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j, desc_sf(sfb_addr + kk * 2048 + 512 * j));
-              tc_cp_pair_32x128b_warpx4(sfb_tmem + 8 * j + 4, desc_sf(sfb_addr + SFB_PANEL + kk * 2048 + 512 * j));
-            }
-            const uint64_t a_desc = desc_sw128(a_addr + kk * KTILE_BYTES), b_desc = desc_sw128(b_addr + kk * KTILE_BYTES);
+            if (kk >= kk_end) break;  // the second k-tile of a last stage past K
+            const uint64_t a_desc = desc_sw128(st + kk * KTILE_BYTES);
+            const uint64_t b_desc = desc_sw128(st + A_BYTES + kk * KTILE_BYTES);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               // K step j: 64 elements = 32 bytes further along the swizzled row
-              tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sfa_tmem + 4 * j,
-                               sfb_tmem + 8 * j, (ks | kk | j) != 0);
+              tc_mma_pair_nvf4(tmem + ACC_COL, a_desc + 2 * j, b_desc + 2 * j, kIdesc, sf_tmem + 4 * (4 * kk + j),
+                               sf_tmem + SFW_COL + 8 * (4 * kk + j), (ks | kk | j) != 0);
             }
           }
-          tc_commit_pair(&sm.empty[stage]);  // frees the stage in both CTAs once these MMAs complete
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          tc_commit_pair(&sm.empty[ab.slot]);  // stage and scale slot reusable in both CTAs
         }
         if (!ok) break;
         tc_commit_pair(sm.tfull);  // accumulators of both CTAs ready
@@ -258,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // in either CTA when the pair tears down.
       tc_commit_pair(sm.mma_done);
     }
-  } else {
+  } else if (warp < WARP_SF0) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
@@ -266,11 +355,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
-      const int mt = t / p.num_n_tiles, nt = t - (t / p.num_n_tiles) * p.num_n_tiles;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(sm.tfull, local & 1, p.wait_limit_cycles, abort_flag);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) {
+      const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
+      if (!warp_wait(sm.tfull, local & 1, p, abort_flag, lane)) {
         if (lane == 0) report_timeout(p, sm.abort_flag);
         break;
       }
@@ -326,6 +412,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
     if (lane == 0) bulk_wait_all();
+  } else {
+    // ------------------------------------------------------------ scale writers (both CTAs)
+    const int q = warp & 3;  // lane quarter: A rows 32q..32q+31 and this quarter's copy of the W scales
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
+    const uint32_t full_leader = mapa_shared(smem_u32(sm.full), 0);
+    const int stages_per_tile = (nk + KT - 1) / KT;
+    // One stage of scale words in registers: the loads for the next stage
+    // are issued as soon as the current one has been stored.
+    ScaleRegs buf;
+    int lt = pair, lks = 0;  // next stage to load
+    auto advance = [&](int& t, int& ks) {
+      if (++ks == stages_per_tile) {
+        ks = 0;
+        t += num_pairs;
+      }
+    };
+    if (lt < num_tiles) {
+      const int mt = lt / p.num_n_tiles;
+      load_scales(buf, p, mt, lt - mt * p.num_n_tiles, lks, rank, q, lane);
+      advance(lt, lks);
+    }
+    Ring r;
+    for (int t = pair, ks = 0; t < num_tiles; advance(t, ks), r.next(STAGES)) {
+      // the stage's slot must no longer be read by earlier MMAs
+      if (!warp_wait(&sm.empty[r.slot], r.phase ^ 1u, p, abort_flag, lane)) {
+        if (lane == 0) report_timeout(p, sm.abort_flag);
+        break;
+      }
+      tc_fence_after();
+      store_scales(tmem + lane_base + SF_COL + uint32_t(r.slot) * SF_SLOT_COLS, buf);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      // relaxed: the stores are complete (wait::st), and a release arrive
+      // would first wait for the prefetch loads still in flight
+      if (lane == 0) mbar_arrive_cluster_relaxed(full_leader + 8u * uint32_t(r.slot));
+      if (lt < num_tiles) {
+        const int mt = lt / p.num_n_tiles;
+        load_scales(buf, p, mt, lt - mt * p.num_n_tiles, lks, rank, q, lane);
+        advance(lt, lks);
+      }
+    }
   }
 
   // teardown: every MMA of the pair has completed before tensor memory is freed
@@ -404,11 +532,9 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
     return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: problem too large");
 
   // A and W: 3-D views [k-tile][row][128 B] so one box carries KT k-tiles of
-  // 128 rows (each a 128B-swizzled 16 KB tile).  Scales: [bytes / 256, 256]
-  // byte rows (one 128-row panel x one k-tile is 8 rows = 2 KB); the W scales
-  // as [panel][row][256] so one box carries both panels of a 256-row tile.
-  const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256;
-  CUtensorMap ta, tw, tsa, tsw, to;
+  // 128 rows (each a 128B-swizzled 16 KB tile).  The block scales are read
+  // by the scale-writer warps straight from the tiled layout.
+  CUtensorMap ta, tw, to;
   nvfp4_status st;
   {
     const cuuint64_t dims[3] = {128, cuuint64_t(m_pad), cuuint64_t(k / 256)};
@@ -427,22 +553,6 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
       return st;
   }
   {
-    const cuuint64_t dims[2] = {256, cuuint64_t(sa_rows)};
-    const cuuint64_t strides[1] = {256};
-    const cuuint32_t box[2] = {256, 8 * KT};
-    if ((st = make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_s, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
-                       "A scales")) != NVFP4_OK)
-      return st;
-  }
-  {
-    const cuuint64_t dims[3] = {256, cuuint64_t(k / 32), cuuint64_t(n / 128)};
-    const cuuint64_t strides[2] = {256, cuuint64_t(k / 32) * 256};
-    const cuuint32_t box[3] = {256, 8 * KT, 2};
-    if ((st = make_map(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
-                       "W scales")) != NVFP4_OK)
-      return st;
-  }
-  {
     const cuuint64_t dims[2] = {cuuint64_t(n), cuuint64_t(m)};
     const cuuint64_t strides[1] = {cuuint64_t(ldo) * 2};
     const cuuint32_t box[2] = {64, 32};
@@ -454,14 +564,16 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   Params prm;
   prm.a_rec = a_rec;
   prm.w_rec = w_rec;
+  prm.a_sf = static_cast<const uint8_t*>(a_s);
+  prm.w_sf = static_cast<const uint8_t*>(w_s);
   prm.a_rows = static_cast<int>(m_pad);
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
   prm.num_n_tiles = static_cast<int>((n + PAIR_N - 1) / PAIR_N);
-  // an odd k-tile count ends with a box whose second k-tile lies beyond K:
-  // the TMA fills it with zeros, which add nothing to the sums
-  prm.num_stages_k = static_cast<int>((k / 256 + KT - 1) / KT);
-  prm.sf_panel_rows = static_cast<int>(k / 32);
+  // an odd k-tile count ends with a stage whose second k-tile lies beyond
+  // K: the TMA fills it with zeros and no MMA reads it
+  prm.num_k_tiles = static_cast<int>(k / 256);
+  prm.sf_blocks = static_cast<int>(k / 64);
   prm.dev_status = dev_status;
   prm.wait_limit_cycles = wait_limit_cycles;
 
@@ -470,7 +582,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, to, prm);
+  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, to, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
