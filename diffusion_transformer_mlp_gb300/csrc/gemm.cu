@@ -12,26 +12,30 @@
 // per instruction); each CTA holds 128 rows of A and 128 rows of W per
 // k-tile and a 128 x 256 FP32 accumulator in its tensor memory.
 //
-//   warp 0      TMA producer (both CTAs): per stage KT k-tiles (256 K
-//               elements each) of this CTA's 128 A rows and 128 W rows
+//   warp 0      operand TMA producer (both CTAs): per stage KT k-tiles (256
+//               K elements each) of this CTA's 128 A rows and 128 W rows
 //               (128B swizzle) into a STAGES-deep shared-memory ring; the
 //               leader's barrier counts both CTAs' bytes.
-//   warp 1      MMA issuer (leader CTA): per stage one wait, 4*KT MMAs
-//               reading the operands from the stage and the block scales
-//               from the stage's tensor-memory slot, one commit; nothing
-//               else goes through the tensor pipe.
-//   warps 2-5   epilogue (both CTAs): tcgen05.ld, multiply by
-//               alpha = gA*gW, round to BF16, stage through 128B-swizzled
-//               shared memory, TMA store (clipped at row M).
-//   warps 6-9   scale writers (both CTAs), one per TMEM lane quarter: read
-//               a stage's UE4M3 words straight from the tiled scale layout
-//               in global memory (one stage ahead, in registers), store them
+//   warp 10     scale TMA producer (both CTAs): per stage this CTA's A
+//               scale blocks and the W scale blocks of both 128-row panels
+//               of the tile (tiled layout, 12 KB) into an SF_RING-deep ring
+//               that runs ahead of the operands.
+//   warps 6-9   scale writers (both CTAs), one per TMEM lane quarter: read a
+//               stage's UE4M3 words from the ring (ld.shared), store them
 //               with tcgen05.st into the stage's tensor-memory slot in the
 //               layout the MMA reads, and arrive on the leader's stage
 //               barrier next to the TMA bytes.  A tcgen05.cp of the scales
 //               would sit in the tensor pipe between the MMAs (a 32x128b
 //               warpx4 copy costs about half an MMA there); tcgen05.st from
 //               other warps does not.
+//   warp 1      MMA issuer (leader CTA): per stage one wait, 4*KT MMAs
+//               reading the operands from the stage and the block scales
+//               from the stage's tensor-memory slot, one commit.
+//   warps 2-5   epilogue (both CTAs): tcgen05.ld 128 accumulator columns at
+//               a time, multiply by alpha = gA*gW, round to BF16, stage
+//               through 128B-swizzled shared memory, TMA store (clipped at
+//               row M); the accumulator goes back to the MMA issuer after
+//               the last load.
 //
 // Tiles are walked M-panel-major (all N tiles of one 256-row panel, then
 // the next), so the CTAs running at any moment share a few activation
@@ -58,17 +62,26 @@ constexpr int KTILE_BYTES = HALF * BK_BYTES;   // 16 KB: 128 rows x one k-tile
 constexpr int A_BYTES = KT * KTILE_BYTES;      // this CTA's 128 A rows x KT k-tiles
 constexpr int B_BYTES = KT * KTILE_BYTES;      // this CTA's 128 W rows x KT k-tiles
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int KSTEPS = 4 * KT;                 // K=64 MMA steps per stage
+// Scale ring: per stage 4*KT blocks of 512 bytes for this CTA's A panel,
+// then the same for W panel 0 and W panel 1 of the tile.
+constexpr int SF_RING = 4;
+constexpr int SFA_BYTES = KSTEPS * 512;
+constexpr int SFW_PANEL_BYTES = KSTEPS * 512;
+constexpr int SF_STAGE_BYTES = SFA_BYTES + 2 * SFW_PANEL_BYTES;  // 12 KB
 constexpr int EPI_WARPS = 4;
 constexpr int SF_WARPS = 4;
 constexpr int WARP_EPI0 = 2;
 constexpr int WARP_SF0 = WARP_EPI0 + EPI_WARPS;
-constexpr int EPI_BYTES = HALF * PAIR_N * 2;   // 128 rows x 256 BF16
+constexpr int WARP_SFP = WARP_SF0 + SF_WARPS;
+constexpr int EPI_COLS = 128;                   // output columns staged per TMA-store round
+constexpr int EPI_BYTES = HALF * EPI_COLS * 2;  // 128 rows x 128 BF16
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-constexpr int THREADS = (WARP_SF0 + SF_WARPS) * 32;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + SF_RING * SF_STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+constexpr int THREADS = (WARP_SFP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;  // 256 FP32 columns
-// Block scales in tensor memory, one slot per operand stage (4*KT K=64
+// Block scales in tensor memory, one slot per operand stage (KSTEPS K=64
 // steps j):
 //   A: step j at column slot + 4j; the scales of accumulator row i are read
 //      from lane i, column slot + 4j + i/32 (the word is stored in all four
@@ -76,14 +89,13 @@ constexpr uint32_t ACC_COL = 0;  // 256 FP32 columns
 //   W: step j at column slot + SFW_COL + 8j; accumulator rows of lane
 //      quarter g read the scales of W row n from lane 32g + n % 32, column
 //      slot + SFW_COL + 8j + n/32, so every quarter holds a copy.
-constexpr int KSTEPS = 4 * KT;  // K=64 steps per stage
 constexpr uint32_t SF_COL = 256;
 constexpr uint32_t SFW_COL = 4 * KSTEPS;
 constexpr uint32_t SF_SLOT_COLS = 12 * KSTEPS;
 static_assert(SF_COL + STAGES * SF_SLOT_COLS <= TMEM_COLS, "tensor memory budget");
 static_assert(KSTEPS == 8, "scale stores are written 32 columns at a time");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(STAGE_BYTES % 1024 == 0, "stage alignment for 128B swizzle");
+static_assert(STAGE_BYTES % 1024 == 0 && SF_STAGE_BYTES % 1024 == 0, "stage alignment");
 
 // Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), both
 // K-major, UE4M3 scales (scale format 0), scale-factor ids 0, N>>3 at bit
@@ -101,10 +113,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 
 struct Smem {
   uint8_t* stage;       // STAGES x [A | B]
-  uint8_t* epi;         // EPI_WARPS x 32 rows x 256 BF16
+  uint8_t* sf;          // SF_RING x [A scales | W scales panel 0 | panel 1]
+  uint8_t* epi;         // EPI_WARPS x 32 rows x EPI_COLS BF16
   uint64_t* full;       // leader: the operand bytes of both CTAs have landed and
                         // the stage's scales are in both CTAs' tensor memory
-  uint64_t* empty;      // each CTA: the stage (operands and scale slot) may be refilled
+  uint64_t* empty;      // each CTA: the stage's MMAs are complete (operands and scale slot free)
+  uint64_t* sf_full;    // each CTA: a scale-ring slot has landed
+  uint64_t* sf_empty;   // each CTA: the scale writers have read a ring slot
   uint64_t* tfull;      // each CTA: accumulators complete
   uint64_t* tempty;     // leader: accumulators of both CTAs drained
   uint64_t* mma_done;
@@ -116,30 +131,31 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   Smem s;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   s.stage = base;
-  s.epi = base + STAGES * STAGE_BYTES;
+  s.sf = base + STAGES * STAGE_BYTES;
+  s.epi = s.sf + SF_RING * SF_STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + EPI_BYTES);
   s.full = bars;
   s.empty = s.full + STAGES;
-  s.tfull = s.empty + STAGES;
+  s.sf_full = s.empty + STAGES;
+  s.sf_empty = s.sf_full + SF_RING;
+  s.tfull = s.sf_empty + SF_RING;
   s.tempty = s.tfull + 1;
   s.mma_done = s.tempty + 1;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   return s;
 }
-static_assert((2 * STAGES + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
+static_assert((2 * STAGES + 2 * SF_RING + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
 
 struct Params {
   const nvfp4_scale_rec* a_rec;
   const nvfp4_scale_rec* w_rec;
-  const uint8_t* a_sf;  // activation block scales, tiled layout
-  const uint8_t* w_sf;  // weight block scales, tiled layout
-  int a_rows;           // padded rows of the activation (multiple of 128)
-  int n;                // weight rows (multiple of 128)
-  int num_m_tiles;      // ceil(a_rows / 256)
-  int num_n_tiles;      // ceil(n / 256)
-  int num_k_tiles;      // k / 256
-  int sf_blocks;        // 512-byte scale blocks per 128-row panel: k / 64
+  int a_rows;        // padded rows of the activation (multiple of 128)
+  int n;             // weight rows (multiple of 128)
+  int num_m_tiles;   // ceil(a_rows / 256)
+  int num_n_tiles;   // ceil(n / 256)
+  int num_k_tiles;   // k / 256
+  int sf_rows;       // 256-byte rows of one 128-row scale panel: k / 32
   uint32_t* dev_status;
   uint64_t wait_limit_cycles;
 };
@@ -170,77 +186,58 @@ struct Ring {
   }
 };
 
-// The scale words one writer lane needs for one stage (K=64 steps
+// The scale words one writer lane stores for one stage (K=64 steps
 // j = 0..KSTEPS-1): lane l of quarter q holds A row 32q + l of this CTA's
 // half (one 32-bit word = four scales per step) and W rows 32c + l of the
 // pair's tile, c = 0..7 (one 16-byte line of the tiled layout per 128-row
-// panel and step).
-struct ScaleRegs {
+// panel and step).  In a ring slot (tiled layout, one 512-byte block per
+// step and panel): the A word at j*512 + 16l + 4q, the W line of panel h at
+// SFA_BYTES + h*SFW_PANEL_BYTES + j*512 + 16l.
+__device__ __forceinline__ void read_and_store_scales(uint32_t taddr, const uint8_t* slot, int q, int lane) {
   uint32_t a[KSTEPS];
   uint4 w[2 * KSTEPS];  // [2j + panel]
-};
-
-__device__ __forceinline__ uint32_t ldg_nc_u32(const uint8_t* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint4 ldg_nc_u128(const uint8_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-// Tiled layout: block (panel, 4-scale column group) of 512 bytes at
-// (panel * sf_blocks + group) * 512; inside it row r of the panel and
-// scale c%4 at (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.  Stage ks,
-// step j is group ks * KSTEPS + j.  Panels past the operand (the second
-// half of a ragged last tile) and steps past K (the second k-tile of a
-// last stage when K / 256 is odd) read as zero scales; the former are
-// never stored, the latter never multiplied.
-__device__ __forceinline__ void load_scales(ScaleRegs& s, const Params& p, int mt, int nt, int ks, uint32_t rank,
-                                            int q, int lane) {
-  const int a_panel = mt * 2 + int(rank);
-  const int w_panel = nt * 2;
-  const int g0 = ks * KSTEPS;
-  const bool a_ok = a_panel * HALF < p.a_rows;
-  const uint8_t* abase = p.a_sf + (size_t(a_panel) * p.sf_blocks + g0) * 512 + lane * 16 + q * 4;
 #pragma unroll
-  for (int j = 0; j < KSTEPS; ++j) s.a[j] = (a_ok && g0 + j < p.sf_blocks) ? ldg_nc_u32(abase + j * 512) : 0u;
+  for (int j = 0; j < KSTEPS; ++j) {
+    a[j] = *reinterpret_cast<const uint32_t*>(slot + j * 512 + lane * 16 + q * 4);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const bool w_ok = (w_panel + h) * HALF < p.n;
-    const uint8_t* wbase = p.w_sf + (size_t(w_panel + h) * p.sf_blocks + g0) * 512 + lane * 16;
-#pragma unroll
-    for (int j = 0; j < KSTEPS; ++j)
-      s.w[2 * j + h] = (w_ok && g0 + j < p.sf_blocks) ? ldg_nc_u128(wbase + j * 512) : make_uint4(0, 0, 0, 0);
+    for (int h = 0; h < 2; ++h)
+      w[2 * j + h] = *reinterpret_cast<const uint4*>(slot + SFA_BYTES + h * SFW_PANEL_BYTES + j * 512 + lane * 16);
   }
-}
-
-__device__ __forceinline__ void store_scales(uint32_t taddr, const ScaleRegs& s) {
-  uint32_t va[32], vw[32];
-#pragma unroll
-  for (int j = 0; j < KSTEPS; ++j) va[4 * j] = va[4 * j + 1] = va[4 * j + 2] = va[4 * j + 3] = s.a[j];
-  tmem_st_32x32b_x32(taddr, va);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%1,%1,%1,%2,%2,%2,%2,%3,%3,%3,%3,%4,%4,%4,%4,"
+      "%5,%5,%5,%5,%6,%6,%6,%6,%7,%7,%7,%7,%8,%8,%8,%8};" ::"r"(taddr),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+      : "memory");
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-#pragma unroll
-    for (int jj = 0; jj < KSTEPS / 2; ++jj) {
-      const int j = half * (KSTEPS / 2) + jj;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        vw[8 * jj + 4 * h + 0] = s.w[2 * j + h].x;
-        vw[8 * jj + 4 * h + 1] = s.w[2 * j + h].y;
-        vw[8 * jj + 4 * h + 2] = s.w[2 * j + h].z;
-        vw[8 * jj + 4 * h + 3] = s.w[2 * j + h].w;
-      }
-    }
-    tmem_st_32x32b_x32(taddr + SFW_COL + 32 * half, vw);
+    const uint4* v = w + 8 * half;
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr + SFW_COL + 32 * half),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w),
+        "r"(v[4].x), "r"(v[4].y), "r"(v[4].z), "r"(v[4].w), "r"(v[5].x), "r"(v[5].y), "r"(v[5].z), "r"(v[5].w),
+        "r"(v[6].x), "r"(v[6].y), "r"(v[6].z), "r"(v[6].w), "r"(v[7].x), "r"(v[7].y), "r"(v[7].z), "r"(v[7].w)
+        : "memory");
   }
 }
+
+// Walk of one CTA pair over its (tile, stage) sequence.
+struct StageWalk {
+  int t, ks;
+  __device__ __forceinline__ void next(int stages_per_tile, int num_pairs) {
+    if (++ks == stages_per_tile) {
+      ks = 0;
+      t += num_pairs;
+    }
+  }
+};
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+               const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
                const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
@@ -251,12 +248,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const volatile int* abort_flag = sm.abort_flag;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int nk = p.num_k_tiles;
+  const int stages_per_tile = (nk + KT - 1) / KT;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // the producer's expect_tx arrival plus one per scale writer of either CTA
       mbar_init(&sm.full[s], 1 + 2 * SF_WARPS);
       mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < SF_RING; ++s) {
+      mbar_init(&sm.sf_full[s], 1);
+      mbar_init(&sm.sf_empty[s], SF_WARPS);
     }
     mbar_init(sm.tfull, 1);
     mbar_init(sm.tempty, 2 * EPI_WARPS);
@@ -265,6 +267,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_sa);
+    prefetch_tmap(&tmap_sw);
     prefetch_tmap(&tmap_out);
   }
   if (warp == 1) tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
@@ -279,34 +283,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_last();
       const uint64_t pol_a = l2_policy_evict_normal();
-      const int stages_per_tile = (nk + KT - 1) / KT;
       Ring r;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
+      for (StageWalk w{pair, 0}; w.t < num_tiles && ok; w.next(stages_per_tile, num_pairs), r.next(STAGES)) {
+        const int mt = w.t / p.num_n_tiles, nt = w.t - mt * p.num_n_tiles;
         // Boxes beyond the operands (the last M or N half, a k-tile past K)
         // are zero-filled by the TMA and still count their full bytes, so
         // every stage carries 2 x STAGE_BYTES for the leader's barrier.
         const int a_row = mt * PAIR_M + int(rank) * HALF;
         const int b_row = nt * PAIR_N + int(rank) * HALF;
-        for (int ks = 0; ks < stages_per_tile; ++ks, r.next(STAGES)) {
-          if (!mbar_wait_bounded(&sm.empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
-            report_timeout(p, sm.abort_flag);
-            ok = false;
-            break;
-          }
-          uint8_t* st = sm.stage + r.slot * STAGE_BYTES;
-          const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[r.slot]), 0);
-          if (leader) mbar_arrive_expect_tx(&sm.full[r.slot], 2 * STAGE_BYTES);
-          tma_load_3d_pair(st, &tmap_a, full_leader, 0, a_row, ks * KT, pol_a);
-          tma_load_3d_pair(st + A_BYTES, &tmap_w, full_leader, 0, b_row, ks * KT, pol_w);
+        if (!mbar_wait_bounded(&sm.empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
+          report_timeout(p, sm.abort_flag);
+          ok = false;
+          break;
         }
+        uint8_t* st = sm.stage + r.slot * STAGE_BYTES;
+        const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[r.slot]), 0);
+        if (leader) mbar_arrive_expect_tx(&sm.full[r.slot], 2 * STAGE_BYTES);
+        tma_load_3d_pair(st, &tmap_a, full_leader, 0, a_row, w.ks * KT, pol_a);
+        tma_load_3d_pair(st + A_BYTES, &tmap_w, full_leader, 0, b_row, w.ks * KT, pol_w);
+      }
+    }
+  } else if (warp == WARP_SFP) {
+    // ------------------------------------------------------------ scale producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_last();
+      const uint64_t pol_a = l2_policy_evict_normal();
+      Ring r;
+      bool ok = true;
+      for (StageWalk w{pair, 0}; w.t < num_tiles && ok; w.next(stages_per_tile, num_pairs), r.next(SF_RING)) {
+        const int mt = w.t / p.num_n_tiles, nt = w.t - mt * p.num_n_tiles;
+        if (!mbar_wait_bounded(&sm.sf_empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
+          report_timeout(p, sm.abort_flag);
+          ok = false;
+          break;
+        }
+        // A scales: 256-byte rows of the whole scale buffer (this CTA's
+        // panel starts at panel * sf_rows); W scales: [panel][row][256].
+        // Rows past K (an odd k-tile count) or past the operand are read
+        // as whatever the box holds or zero fill and never multiplied or
+        // stored.
+        uint8_t* sl = sm.sf + r.slot * SF_STAGE_BYTES;
+        const int row0 = w.ks * KSTEPS * 2;  // two 256-byte rows per 512-byte block
+        mbar_arrive_expect_tx(&sm.sf_full[r.slot], SF_STAGE_BYTES);
+        tma_load_2d(sl, &tmap_sa, &sm.sf_full[r.slot], 0, (mt * 2 + int(rank)) * p.sf_rows + row0, pol_a);
+        tma_load_3d(sl + SFA_BYTES, &tmap_sw, &sm.sf_full[r.slot], 0, row0, nt * 2, pol_w);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      const int stages_per_tile = (nk + KT - 1) / KT;
       Ring ab;
       int local = 0;
       bool ok = true;
@@ -338,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                sf_tmem + SFW_COL + 8 * (4 * kk + j), (ks | kk | j) != 0);
             }
           }
-          tc_commit_pair(&sm.empty[ab.slot]);  // stage and scale slot reusable in both CTAs
+          tc_commit_pair(&sm.empty[ab.slot]);  // stage and its scale slot reusable in both CTAs
         }
         if (!ok) break;
         tc_commit_pair(sm.tfull);  // accumulators of both CTAs ready
@@ -351,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
-    uint8_t* stg = sm.epi + q * (32 * PAIR_N * 2);
+    uint8_t* stg = sm.epi + q * (32 * EPI_COLS * 2);
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
@@ -361,54 +387,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      if (lane == 0) bulk_wait_read_all();  // previous stores have read the staging buffer
-      __syncwarp();
+      // Row `lane` of this quarter, EPI_COLS columns at a time: TMEM ->
+      // registers (BF16 pairs) -> 128B-swizzled staging -> TMA store.  The
+      // accumulator goes back to the MMA issuer right after the last load.
       const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL;
+      const int y = mt * PAIR_M + int(rank) * HALF + q * 32;
 #pragma unroll 1
-      for (int c = 0; c < PAIR_N / 32; ++c) {
-        uint32_t r[32];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(row_tmem + c * 32));
-        tc_wait_ld();
-        // row `lane` of this quarter, columns 32c..32c+31 -> 4 chunks of 16 B
-        uint8_t* sub = stg + (c >> 1) * (32 * 128) + lane * 128;
+      for (int h = 0; h < PAIR_N / EPI_COLS; ++h) {
+        uint32_t packed[EPI_COLS / 2];
 #pragma unroll
-        for (int t4 = 0; t4 < 4; ++t4) {
-          uint32_t w[4];
+        for (int c = 0; c < EPI_COLS / 32; ++c) {
+          uint32_t r[32];
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+              "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+              : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+              : "r"(row_tmem + h * EPI_COLS + c * 32));
+          tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float lo = __fmul_rn(__uint_as_float(r[t4 * 8 + 2 * i]), alpha);
-            const float hi = __fmul_rn(__uint_as_float(r[t4 * 8 + 2 * i + 1]), alpha);
-            w[i] = bf16x2_rn(lo, hi);
-          }
-          const int chunk = ((c & 1) * 4 + t4) ^ (lane & 7);
-          *reinterpret_cast<uint4*>(sub + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int i = 0; i < 16; ++i)
+            packed[c * 16 + i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
+                                           __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
         }
-      }
-      // accumulator drained: hand it back to the MMA issuer of the pair
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int y = mt * PAIR_M + int(rank) * HALF + q * 32;
-        if (y < p.a_rows) {
-#pragma unroll
-          for (int h = 0; h < PAIR_N / 64; ++h) {
-            const int x = nt * PAIR_N + h * 64;
-            if (x < p.n) tma_store_2d(&tmap_out, stg + h * (32 * 128), x, y);
-          }
+        if (h == PAIR_N / EPI_COLS - 1) {
+          // accumulator drained: hand it back to the MMA issuer of the pair
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_leader);
         }
-        bulk_commit();
+        if (lane == 0) bulk_wait_read_all();  // earlier stores have read the staging buffer
+        __syncwarp();
+        // row `lane`, EPI_COLS columns = sub-tiles of 64 (128-byte rows, 128B swizzle)
+#pragma unroll
+        for (int ch = 0; ch < EPI_COLS / 8; ++ch) {
+          const int sub = ch >> 3, c16 = ch & 7;
+          uint8_t* dst = stg + sub * (32 * 128) + lane * 128 + ((c16 ^ (lane & 7)) * 16);
+          const int b = ch * 4;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(packed[b], packed[b + 1], packed[b + 2], packed[b + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (y < p.a_rows) {
+#pragma unroll
+            for (int sub = 0; sub < EPI_COLS / 64; ++sub) {
+              const int x = nt * PAIR_N + h * EPI_COLS + sub * 64;
+              if (x < p.n) tma_store_2d(&tmap_out, stg + sub * (32 * 128), x, y);
+            }
+          }
+          bulk_commit();
+        }
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -417,42 +450,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // lane quarter: A rows 32q..32q+31 and this quarter's copy of the W scales
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     const uint32_t full_leader = mapa_shared(smem_u32(sm.full), 0);
-    const int stages_per_tile = (nk + KT - 1) / KT;
-    // One stage of scale words in registers: the loads for the next stage
-    // are issued as soon as the current one has been stored.
-    ScaleRegs buf;
-    int lt = pair, lks = 0;  // next stage to load
-    auto advance = [&](int& t, int& ks) {
-      if (++ks == stages_per_tile) {
-        ks = 0;
-        t += num_pairs;
-      }
-    };
-    if (lt < num_tiles) {
-      const int mt = lt / p.num_n_tiles;
-      load_scales(buf, p, mt, lt - mt * p.num_n_tiles, lks, rank, q, lane);
-      advance(lt, lks);
-    }
-    Ring r;
-    for (int t = pair, ks = 0; t < num_tiles; advance(t, ks), r.next(STAGES)) {
-      // the stage's slot must no longer be read by earlier MMAs
-      if (!warp_wait(&sm.empty[r.slot], r.phase ^ 1u, p, abort_flag, lane)) {
+    Ring r;   // operand stage (its full barrier and tensor-memory scale slot)
+    Ring sr;  // scale ring slot
+    for (StageWalk w{pair, 0}; w.t < num_tiles; w.next(stages_per_tile, num_pairs), r.next(STAGES), sr.next(SF_RING)) {
+      // the ring slot has landed and the stage's tensor-memory slot is no
+      // longer read by the MMAs of the stage STAGES back
+      if (!warp_wait(&sm.sf_full[sr.slot], sr.phase, p, abort_flag, lane) ||
+          !warp_wait(&sm.empty[r.slot], r.phase ^ 1u, p, abort_flag, lane)) {
         if (lane == 0) report_timeout(p, sm.abort_flag);
         break;
       }
       tc_fence_after();
-      store_scales(tmem + lane_base + SF_COL + uint32_t(r.slot) * SF_SLOT_COLS, buf);
+      read_and_store_scales(tmem + lane_base + SF_COL + uint32_t(r.slot) * SF_SLOT_COLS,
+                            sm.sf + sr.slot * SF_STAGE_BYTES, q, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.sf_empty[sr.slot]);  // ring slot read
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      // relaxed: the stores are complete (wait::st), and a release arrive
-      // would first wait for the prefetch loads still in flight
+      // relaxed: the stores are complete (wait::st); nothing else needs ordering
       if (lane == 0) mbar_arrive_cluster_relaxed(full_leader + 8u * uint32_t(r.slot));
-      if (lt < num_tiles) {
-        const int mt = lt / p.num_n_tiles;
-        load_scales(buf, p, mt, lt - mt * p.num_n_tiles, lks, rank, q, lane);
-        advance(lt, lks);
-      }
     }
   }
 
@@ -532,9 +549,12 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
     return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: problem too large");
 
   // A and W: 3-D views [k-tile][row][128 B] so one box carries KT k-tiles of
-  // 128 rows (each a 128B-swizzled 16 KB tile).  The block scales are read
-  // by the scale-writer warps straight from the tiled layout.
-  CUtensorMap ta, tw, to;
+  // 128 rows (each a 128B-swizzled 16 KB tile).  Scales: the A scales as
+  // [bytes / 256][256] (one 128-row panel x one k-tile is 8 rows = 2 KB),
+  // the W scales as [panel][k / 32][256] so one box carries a stage of both
+  // panels of a 256-row tile.
+  const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256;
+  CUtensorMap ta, tw, tsa, tsw, to;
   nvfp4_status st;
   {
     const cuuint64_t dims[3] = {128, cuuint64_t(m_pad), cuuint64_t(k / 256)};
@@ -553,6 +573,22 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
       return st;
   }
   {
+    const cuuint64_t dims[2] = {256, cuuint64_t(sa_rows)};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {256, 2 * KSTEPS};
+    if ((st = make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_s, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       "A scales")) != NVFP4_OK)
+      return st;
+  }
+  {
+    const cuuint64_t dims[3] = {256, cuuint64_t(k / 32), cuuint64_t(n / 128)};
+    const cuuint64_t strides[2] = {256, cuuint64_t(k / 32) * 256};
+    const cuuint32_t box[3] = {256, 2 * KSTEPS, 2};
+    if ((st = make_map(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       "W scales")) != NVFP4_OK)
+      return st;
+  }
+  {
     const cuuint64_t dims[2] = {cuuint64_t(n), cuuint64_t(m)};
     const cuuint64_t strides[1] = {cuuint64_t(ldo) * 2};
     const cuuint32_t box[2] = {64, 32};
@@ -564,8 +600,6 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   Params prm;
   prm.a_rec = a_rec;
   prm.w_rec = w_rec;
-  prm.a_sf = static_cast<const uint8_t*>(a_s);
-  prm.w_sf = static_cast<const uint8_t*>(w_s);
   prm.a_rows = static_cast<int>(m_pad);
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
@@ -573,7 +607,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   // an odd k-tile count ends with a stage whose second k-tile lies beyond
   // K: the TMA fills it with zeros and no MMA reads it
   prm.num_k_tiles = static_cast<int>(k / 256);
-  prm.sf_blocks = static_cast<int>(k / 64);
+  prm.sf_rows = static_cast<int>(k / 32);
   prm.dev_status = dev_status;
   prm.wait_limit_cycles = wait_limit_cycles;
 
@@ -582,7 +616,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, to, prm);
+  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, to, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
