@@ -15,14 +15,17 @@
 //   warp 0      operand TMA producer (both CTAs): per stage KT k-tiles (256
 //               K elements each) of this CTA's 128 A rows and 128 W rows
 //               (128B swizzle) into a STAGES-deep shared-memory ring; the
-//               leader's barrier counts both CTAs' bytes.
+//               leader's barrier counts both CTAs' bytes.  A 64 KB stage
+//               takes ~1,800 cycles to land against ~1,100 cycles of MMAs,
+//               so three stages are in flight.
 //   warp 10     scale TMA producer (both CTAs): per stage this CTA's A
 //               scale blocks and the W scale blocks of both 128-row panels
 //               of the tile (tiled layout, 12 KB) into an SF_RING-deep ring
 //               that runs ahead of the operands.
 //   warps 6-9   scale writers (both CTAs), one per TMEM lane quarter: read a
 //               stage's UE4M3 words from the ring (ld.shared), store them
-//               with tcgen05.st into the stage's tensor-memory slot in the
+//               with tcgen05.st into one of two tensor-memory slots (free
+//               once the MMAs of the stage two back have completed) in the
 //               layout the MMA reads, and arrive on the leader's stage
 //               barrier next to the TMA bytes.  A tcgen05.cp of the scales
 //               would sit in the tensor pipe between the MMAs (a 32x128b
@@ -31,11 +34,12 @@
 //   warp 1      MMA issuer (leader CTA): per stage one wait, 4*KT MMAs
 //               reading the operands from the stage and the block scales
 //               from the stage's tensor-memory slot, one commit.
-//   warps 2-5   epilogue (both CTAs): tcgen05.ld 128 accumulator columns at
-//               a time, multiply by alpha = gA*gW, round to BF16, stage
-//               through 128B-swizzled shared memory, TMA store (clipped at
-//               row M); the accumulator goes back to the MMA issuer after
-//               the last load.
+//   warps 2-5   epilogue (both CTAs): tcgen05.ld 32 accumulator columns at
+//               a time, multiply by alpha = gA*gW, round to BF16 and store
+//               the row's 64 bytes straight to global memory (rows < M,
+//               columns < N); the accumulator goes back to the MMA issuer
+//               after the last load.  No shared-memory staging: the operand
+//               ring needs the space.
 //
 // Tiles are walked M-panel-major (all N tiles of one 256-row panel, then
 // the next), so the CTAs running at any moment share a few activation
@@ -57,7 +61,7 @@ constexpr int PAIR_N = 256;
 constexpr int HALF = 128;
 constexpr int BK_BYTES = 128;  // 256 E2M1 elements per k-tile
 constexpr int KT = 2;          // k-tiles per pipeline stage (one TMA box per operand per stage)
-constexpr int STAGES = 2;
+constexpr int STAGES = 3;
 constexpr int KTILE_BYTES = HALF * BK_BYTES;   // 16 KB: 128 rows x one k-tile
 constexpr int A_BYTES = KT * KTILE_BYTES;      // this CTA's 128 A rows x KT k-tiles
 constexpr int B_BYTES = KT * KTILE_BYTES;      // this CTA's 128 W rows x KT k-tiles
@@ -65,7 +69,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int KSTEPS = 4 * KT;                 // K=64 MMA steps per stage
 // Scale ring: per stage 4*KT blocks of 512 bytes for this CTA's A panel,
 // then the same for W panel 0 and W panel 1 of the tile.
-constexpr int SF_RING = 4;
+constexpr int SF_RING = 2;
 constexpr int SFA_BYTES = KSTEPS * 512;
 constexpr int SFW_PANEL_BYTES = KSTEPS * 512;
 constexpr int SF_STAGE_BYTES = SFA_BYTES + 2 * SFW_PANEL_BYTES;  // 12 KB
@@ -74,15 +78,13 @@ constexpr int SF_WARPS = 4;
 constexpr int WARP_EPI0 = 2;
 constexpr int WARP_SF0 = WARP_EPI0 + EPI_WARPS;
 constexpr int WARP_SFP = WARP_SF0 + SF_WARPS;
-constexpr int EPI_COLS = 128;                   // output columns staged per TMA-store round
-constexpr int EPI_BYTES = HALF * EPI_COLS * 2;  // 128 rows x 128 BF16
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + SF_RING * SF_STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + SF_RING * SF_STAGE_BYTES + BAR_BYTES;
 constexpr int THREADS = (WARP_SFP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;  // 256 FP32 columns
-// Block scales in tensor memory, one slot per operand stage (KSTEPS K=64
-// steps j):
+// Block scales in tensor memory, two slots used by alternate stages
+// (KSTEPS K=64 steps j each):
 //   A: step j at column slot + 4j; the scales of accumulator row i are read
 //      from lane i, column slot + 4j + i/32 (the word is stored in all four
 //      columns).
@@ -92,7 +94,9 @@ constexpr uint32_t ACC_COL = 0;  // 256 FP32 columns
 constexpr uint32_t SF_COL = 256;
 constexpr uint32_t SFW_COL = 4 * KSTEPS;
 constexpr uint32_t SF_SLOT_COLS = 12 * KSTEPS;
-static_assert(SF_COL + STAGES * SF_SLOT_COLS <= TMEM_COLS, "tensor memory budget");
+constexpr int SF_SLOTS = 2;
+static_assert(SF_COL + SF_SLOTS * SF_SLOT_COLS <= TMEM_COLS, "tensor memory budget");
+static_assert(STAGES > SF_SLOTS, "a stage's scale slot is free once the stage SF_SLOTS back has completed");
 static_assert(KSTEPS == 8, "scale stores are written 32 columns at a time");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0 && SF_STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -114,10 +118,9 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 struct Smem {
   uint8_t* stage;       // STAGES x [A | B]
   uint8_t* sf;          // SF_RING x [A scales | W scales panel 0 | panel 1]
-  uint8_t* epi;         // EPI_WARPS x 32 rows x EPI_COLS BF16
   uint64_t* full;       // leader: the operand bytes of both CTAs have landed and
                         // the stage's scales are in both CTAs' tensor memory
-  uint64_t* empty;      // each CTA: the stage's MMAs are complete (operands and scale slot free)
+  uint64_t* empty;      // each CTA: the stage's MMAs are complete (operands and its scale slot free)
   uint64_t* sf_full;    // each CTA: a scale-ring slot has landed
   uint64_t* sf_empty;   // each CTA: the scale writers have read a ring slot
   uint64_t* tfull;      // each CTA: accumulators complete
@@ -132,8 +135,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   s.stage = base;
   s.sf = base + STAGES * STAGE_BYTES;
-  s.epi = s.sf + SF_RING * SF_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + EPI_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.sf + SF_RING * SF_STAGE_BYTES);
   s.full = bars;
   s.empty = s.full + STAGES;
   s.sf_full = s.empty + STAGES;
@@ -150,6 +152,9 @@ static_assert((2 * STAGES + 2 * SF_RING + 3) * 8 + 8 <= BAR_BYTES, "barrier area
 struct Params {
   const nvfp4_scale_rec* a_rec;
   const nvfp4_scale_rec* w_rec;
+  __nv_bfloat16* out;  // [m, ldo] row-major
+  int64_t ldo;
+  int m;             // output rows
   int a_rows;        // padded rows of the activation (multiple of 128)
   int n;             // weight rows (multiple of 128)
   int num_m_tiles;   // ceil(a_rows / 256)
@@ -193,33 +198,39 @@ struct Ring {
 // panel and step).  In a ring slot (tiled layout, one 512-byte block per
 // step and panel): the A word at j*512 + 16l + 4q, the W line of panel h at
 // SFA_BYTES + h*SFW_PANEL_BYTES + j*512 + 16l.
-__device__ __forceinline__ void read_and_store_scales(uint32_t taddr, const uint8_t* slot, int q, int lane) {
+struct ScaleWords {
   uint32_t a[KSTEPS];
   uint4 w[2 * KSTEPS];  // [2j + panel]
+};
+
+__device__ __forceinline__ void read_scales(ScaleWords& v, const uint8_t* slot, int q, int lane) {
 #pragma unroll
   for (int j = 0; j < KSTEPS; ++j) {
-    a[j] = *reinterpret_cast<const uint32_t*>(slot + j * 512 + lane * 16 + q * 4);
+    v.a[j] = *reinterpret_cast<const uint32_t*>(slot + j * 512 + lane * 16 + q * 4);
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      w[2 * j + h] = *reinterpret_cast<const uint4*>(slot + SFA_BYTES + h * SFW_PANEL_BYTES + j * 512 + lane * 16);
+      v.w[2 * j + h] = *reinterpret_cast<const uint4*>(slot + SFA_BYTES + h * SFW_PANEL_BYTES + j * 512 + lane * 16);
   }
+}
+
+__device__ __forceinline__ void store_scales(uint32_t taddr, const ScaleWords& v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%1,%1,%1,%2,%2,%2,%2,%3,%3,%3,%3,%4,%4,%4,%4,"
       "%5,%5,%5,%5,%6,%6,%6,%6,%7,%7,%7,%7,%8,%8,%8,%8};" ::"r"(taddr),
-      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+      "r"(v.a[0]), "r"(v.a[1]), "r"(v.a[2]), "r"(v.a[3]), "r"(v.a[4]), "r"(v.a[5]), "r"(v.a[6]), "r"(v.a[7])
       : "memory");
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    const uint4* v = w + 8 * half;
+    const uint4* x = v.w + 8 * half;
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr + SFW_COL + 32 * half),
-        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
-        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w),
-        "r"(v[4].x), "r"(v[4].y), "r"(v[4].z), "r"(v[4].w), "r"(v[5].x), "r"(v[5].y), "r"(v[5].z), "r"(v[5].w),
-        "r"(v[6].x), "r"(v[6].y), "r"(v[6].z), "r"(v[6].w), "r"(v[7].x), "r"(v[7].y), "r"(v[7].z), "r"(v[7].w)
+        "r"(x[0].x), "r"(x[0].y), "r"(x[0].z), "r"(x[0].w), "r"(x[1].x), "r"(x[1].y), "r"(x[1].z), "r"(x[1].w),
+        "r"(x[2].x), "r"(x[2].y), "r"(x[2].z), "r"(x[2].w), "r"(x[3].x), "r"(x[3].y), "r"(x[3].z), "r"(x[3].w),
+        "r"(x[4].x), "r"(x[4].y), "r"(x[4].z), "r"(x[4].w), "r"(x[5].x), "r"(x[5].y), "r"(x[5].z), "r"(x[5].w),
+        "r"(x[6].x), "r"(x[6].y), "r"(x[6].z), "r"(x[6].w), "r"(x[7].x), "r"(x[7].y), "r"(x[7].z), "r"(x[7].w)
         : "memory");
   }
 }
@@ -238,7 +249,7 @@ struct StageWalk {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
-               const __grid_constant__ CUtensorMap tmap_out, const Params p) {
+               const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,7 +280,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_sa);
     prefetch_tmap(&tmap_sw);
-    prefetch_tmap(&tmap_out);
   }
   if (warp == 1) tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -334,6 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
       Ring ab;
+      int sf_slot = 0;
       int local = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs, ++local) {
@@ -342,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < stages_per_tile; ++ks, ab.next(STAGES)) {
+        for (int ks = 0; ks < stages_per_tile; ++ks, ab.next(STAGES), sf_slot ^= 1) {
           if (!mbar_wait_bounded(&sm.full[ab.slot], ab.phase, p.wait_limit_cycles, abort_flag)) {
             report_timeout(p, sm.abort_flag);
             ok = false;
@@ -350,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t st = smem_u32(sm.stage + ab.slot * STAGE_BYTES);
-          const uint32_t sf_tmem = tmem + SF_COL + uint32_t(ab.slot) * SF_SLOT_COLS;
+          const uint32_t sf_tmem = tmem + SF_COL + uint32_t(sf_slot) * SF_SLOT_COLS;
           const int kk_end = (ks * KT + KT <= nk) ? KT : nk - ks * KT;
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
@@ -377,7 +388,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
-    uint8_t* stg = sm.epi + q * (32 * EPI_COLS * 2);
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
@@ -387,88 +397,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      // Row `lane` of this quarter, EPI_COLS columns at a time: TMEM ->
-      // registers (BF16 pairs) -> 128B-swizzled staging -> TMA store.  The
-      // accumulator goes back to the MMA issuer right after the last load.
+      // Row `lane` of this quarter, 32 columns at a time: TMEM -> registers
+      // -> BF16 pairs -> four 16-byte stores (the next chunk's stores fill
+      // the other half of each 32-byte sector).
       const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL;
-      const int y = mt * PAIR_M + int(rank) * HALF + q * 32;
+      const int row = mt * PAIR_M + int(rank) * HALF + q * 32 + lane;
+      const bool row_ok = row < p.m;
+      __nv_bfloat16* orow = p.out + int64_t(row_ok ? row : 0) * p.ldo + nt * PAIR_N;
+      const int cols = p.n - nt * PAIR_N < PAIR_N ? p.n - nt * PAIR_N : PAIR_N;
 #pragma unroll 1
-      for (int h = 0; h < PAIR_N / EPI_COLS; ++h) {
-        uint32_t packed[EPI_COLS / 2];
-#pragma unroll
-        for (int c = 0; c < EPI_COLS / 32; ++c) {
-          uint32_t r[32];
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-              "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-              : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-                "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-                "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-              : "r"(row_tmem + h * EPI_COLS + c * 32));
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[c * 16 + i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
-                                           __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
-        }
-        if (h == PAIR_N / EPI_COLS - 1) {
+      for (int c = 0; c < PAIR_N / 32; ++c) {
+        uint32_t r[32];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(row_tmem + c * 32));
+        tc_wait_ld();
+        if (c == PAIR_N / 32 - 1) {
           // accumulator drained: hand it back to the MMA issuer of the pair
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty_leader);
+          // the loads are complete (wait::ld, fence::before_thread_sync);
+          // a release would also wait for this row's global stores
+          if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
         }
-        if (lane == 0) bulk_wait_read_all();  // earlier stores have read the staging buffer
-        __syncwarp();
-        // row `lane`, EPI_COLS columns = sub-tiles of 64 (128-byte rows, 128B swizzle)
+        uint32_t w[16];
 #pragma unroll
-        for (int ch = 0; ch < EPI_COLS / 8; ++ch) {
-          const int sub = ch >> 3, c16 = ch & 7;
-          uint8_t* dst = stg + sub * (32 * 128) + lane * 128 + ((c16 ^ (lane & 7)) * 16);
-          const int b = ch * 4;
-          *reinterpret_cast<uint4*>(dst) = make_uint4(packed[b], packed[b + 1], packed[b + 2], packed[b + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (y < p.a_rows) {
+        for (int i = 0; i < 16; ++i)
+          w[i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha), __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+        if (row_ok && c * 32 < cols) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-            for (int sub = 0; sub < EPI_COLS / 64; ++sub) {
-              const int x = nt * PAIR_N + h * EPI_COLS + sub * 64;
-              if (x < p.n) tma_store_2d(&tmap_out, stg + sub * (32 * 128), x, y);
-            }
-          }
-          bulk_commit();
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
     }
-    if (lane == 0) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ scale writers (both CTAs)
     const int q = warp & 3;  // lane quarter: A rows 32q..32q+31 and this quarter's copy of the W scales
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     const uint32_t full_leader = mapa_shared(smem_u32(sm.full), 0);
-    Ring r;   // operand stage (its full barrier and tensor-memory scale slot)
-    Ring sr;  // scale ring slot
-    for (StageWalk w{pair, 0}; w.t < num_tiles; w.next(stages_per_tile, num_pairs), r.next(STAGES), sr.next(SF_RING)) {
-      // the ring slot has landed and the stage's tensor-memory slot is no
-      // longer read by the MMAs of the stage STAGES back
-      if (!warp_wait(&sm.sf_full[sr.slot], sr.phase, p, abort_flag, lane) ||
-          !warp_wait(&sm.empty[r.slot], r.phase ^ 1u, p, abort_flag, lane)) {
+    Ring r;     // operand stage (its full barrier)
+    Ring back;  // the stage SF_SLOTS back, whose MMAs free this stage's tensor-memory scale slot
+    Ring sr;    // scale ring slot
+    int g = 0;  // stages handled by this pair so far
+    int sf_slot = 0;
+    for (StageWalk w{pair, 0}; w.t < num_tiles;
+         w.next(stages_per_tile, num_pairs), r.next(STAGES), sr.next(SF_RING), sf_slot ^= 1, ++g) {
+      if (!warp_wait(&sm.sf_full[sr.slot], sr.phase, p, abort_flag, lane)) {
         if (lane == 0) report_timeout(p, sm.abort_flag);
         break;
       }
-      tc_fence_after();
-      read_and_store_scales(tmem + lane_base + SF_COL + uint32_t(r.slot) * SF_SLOT_COLS,
-                            sm.sf + sr.slot * SF_STAGE_BYTES, q, lane);
+      // Read the ring slot into registers and release it, then wait for
+      // the tensor-memory slot (the first SF_SLOTS stages find it free).
+      // The next TMA into the slot writes through the async proxy: the
+      // proxy fence orders these generic-proxy reads before it (without it
+      // the refill was seen to race the reads).
+      ScaleWords v;
+      read_scales(v, sm.sf + sr.slot * SF_STAGE_BYTES, q, lane);
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.sf_empty[sr.slot]);  // ring slot read
+      if (lane == 0) mbar_arrive(&sm.sf_empty[sr.slot]);
+      if (g >= SF_SLOTS) {
+        if (!warp_wait(&sm.empty[back.slot], back.phase, p, abort_flag, lane)) {
+          if (lane == 0) report_timeout(p, sm.abort_flag);
+          break;
+        }
+        back.next(STAGES);
+      }
+      tc_fence_after();
+      store_scales(tmem + lane_base + SF_COL + uint32_t(sf_slot) * SF_SLOT_COLS, v);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      // relaxed: the stores are complete (wait::st); nothing else needs ordering
+      // the stores are complete (wait::st, fence::before_thread_sync)
       if (lane == 0) mbar_arrive_cluster_relaxed(full_leader + 8u * uint32_t(r.slot));
     }
   }
@@ -554,7 +562,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   // the W scales as [panel][k / 32][256] so one box carries a stage of both
   // panels of a 256-row tile.
   const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256;
-  CUtensorMap ta, tw, tsa, tsw, to;
+  CUtensorMap ta, tw, tsa, tsw;
   nvfp4_status st;
   {
     const cuuint64_t dims[3] = {128, cuuint64_t(m_pad), cuuint64_t(k / 256)};
@@ -588,18 +596,12 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
                        "W scales")) != NVFP4_OK)
       return st;
   }
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(n), cuuint64_t(m)};
-    const cuuint64_t strides[1] = {cuuint64_t(ldo) * 2};
-    const cuuint32_t box[2] = {64, 32};
-    if ((st = make_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                       "out")) != NVFP4_OK)
-      return st;
-  }
-
   Params prm;
   prm.a_rec = a_rec;
   prm.w_rec = w_rec;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.ldo = ldo;
+  prm.m = static_cast<int>(m);
   prm.a_rows = static_cast<int>(m_pad);
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
@@ -616,7 +618,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, to, prm);
+  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
