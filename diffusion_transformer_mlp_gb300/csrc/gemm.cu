@@ -18,11 +18,11 @@
 //               leader's barrier counts both CTAs' bytes.  A 64 KB stage
 //               takes ~1,800 cycles to land against ~1,100 cycles of MMAs,
 //               so three stages are in flight.
-//   warp 10     scale TMA producer (both CTAs): per stage this CTA's A
+//   warp 14     scale TMA producer (both CTAs): per stage this CTA's A
 //               scale blocks and the W scale blocks of both 128-row panels
 //               of the tile (tiled layout, 12 KB) into an SF_RING-deep ring
 //               that runs ahead of the operands.
-//   warps 6-9   scale writers (both CTAs), one per TMEM lane quarter: read a
+//   warps 10-13 scale writers (both CTAs), one per TMEM lane quarter: read a
 //               stage's UE4M3 words from the ring (ld.shared), store them
 //               with tcgen05.st into one of two tensor-memory slots (free
 //               once the MMAs of the stage two back have completed) in the
@@ -34,12 +34,15 @@
 //   warp 1      MMA issuer (leader CTA): per stage one wait, 4*KT MMAs
 //               reading the operands from the stage and the block scales
 //               from the stage's tensor-memory slot, one commit.
-//   warps 2-5   epilogue (both CTAs): tcgen05.ld 32 accumulator columns at
-//               a time, multiply by alpha = gA*gW, round to BF16 and store
-//               the row's 64 bytes straight to global memory (rows < M,
-//               columns < N); the accumulator goes back to the MMA issuer
-//               after the last load.  No shared-memory staging: the operand
-//               ring needs the space.
+//   warps 2-9   epilogue (both CTAs), two warps per TMEM lane quarter, 128
+//               columns each: tcgen05.ld 32 accumulator columns at a time,
+//               multiply by alpha = gA*gW, round to BF16 and store the
+//               row's 64 bytes straight to global memory as two 32-byte
+//               (whole-sector) stores (rows < M, columns < N); the
+//               accumulator goes back to the MMA issuer after the last
+//               load.  No shared-memory staging: the operand ring needs
+//               the space.  The issuer waits for this drain at every tile
+//               boundary, hence eight warps.
 //
 // Tiles are walked M-panel-major (all N tiles of one 256-row panel, then
 // the next), so the CTAs running at any moment share a few activation
@@ -73,7 +76,7 @@ constexpr int SF_RING = 2;
 constexpr int SFA_BYTES = KSTEPS * 512;
 constexpr int SFW_PANEL_BYTES = KSTEPS * 512;
 constexpr int SF_STAGE_BYTES = SFA_BYTES + 2 * SFW_PANEL_BYTES;  // 12 KB
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, 128 columns each
 constexpr int SF_WARPS = 4;
 constexpr int WARP_EPI0 = 2;
 constexpr int WARP_SF0 = WARP_EPI0 + EPI_WARPS;
@@ -154,6 +157,7 @@ struct Params {
   const nvfp4_scale_rec* w_rec;
   __nv_bfloat16* out;  // [m, ldo] row-major
   int64_t ldo;
+  int store32;       // out is 32-byte aligned and ldo a multiple of 16: 32-byte stores
   int m;             // output rows
   int a_rows;        // padded rows of the activation (multiple of 128)
   int n;             // weight rows (multiple of 128)
@@ -387,6 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp < WARP_SF0) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int col0 = ((warp - WARP_EPI0) / 4) * (PAIR_N / 2);  // this warp's half of the columns
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
     int local = 0;
@@ -397,16 +402,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      // Row `lane` of this quarter, 32 columns at a time: TMEM -> registers
-      // -> BF16 pairs -> four 16-byte stores (the next chunk's stores fill
-      // the other half of each 32-byte sector).
-      const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL;
+      // Row `lane` of this quarter, columns col0..col0+127, 32 at a time:
+      // TMEM -> registers -> BF16 pairs -> four 16-byte stores (the next
+      // chunk's stores fill the other half of each 32-byte sector).
+      const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL + col0;
       const int row = mt * PAIR_M + int(rank) * HALF + q * 32 + lane;
       const bool row_ok = row < p.m;
-      __nv_bfloat16* orow = p.out + int64_t(row_ok ? row : 0) * p.ldo + nt * PAIR_N;
-      const int cols = p.n - nt * PAIR_N < PAIR_N ? p.n - nt * PAIR_N : PAIR_N;
+      __nv_bfloat16* orow = p.out + int64_t(row_ok ? row : 0) * p.ldo + nt * PAIR_N + col0;
+      const int cols = p.n - nt * PAIR_N - col0;  // columns of this half inside N (may be <= 0)
 #pragma unroll 1
-      for (int c = 0; c < PAIR_N / 32; ++c) {
+      for (int c = 0; c < PAIR_N / 64; ++c) {
         uint32_t r[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -419,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
             : "r"(row_tmem + c * 32));
         tc_wait_ld();
-        if (c == PAIR_N / 32 - 1) {
+        if (c == PAIR_N / 64 - 1) {
           // accumulator drained: hand it back to the MMA issuer of the pair
           tc_fence_before();
           __syncwarp();
@@ -432,9 +437,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int i = 0; i < 16; ++i)
           w[i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha), __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
         if (row_ok && c * 32 < cols) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          __nv_bfloat16* dst = orow + c * 32;
+          if (p.store32) {
+            // two 32-byte stores: each lane writes whole sectors (the
+            // scattered 16-byte form cost ~0.065 ms on the canonical case)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int h = 0; h < 2; ++h)
+              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * h), "r"(w[8 * h]),
+                           "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                           "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                           : "memory");
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
       }
     }
@@ -601,6 +618,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   prm.w_rec = w_rec;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.ldo = ldo;
+  prm.store32 = (reinterpret_cast<uintptr_t>(out) % 32 == 0 && ldo % 16 == 0) ? 1 : 0;
   prm.m = static_cast<int>(m);
   prm.a_rows = static_cast<int>(m_pad);
   prm.n = static_cast<int>(n);
