@@ -411,20 +411,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __nv_bfloat16* orow = p.out + int64_t(row_ok ? row : 0) * p.ldo + nt * PAIR_N + col0;
       const int cols = p.n - nt * PAIR_N - col0;  // columns of this half inside N (may be <= 0)
 #pragma unroll 1
-      for (int c = 0; c < PAIR_N / 64; ++c) {
-        uint32_t r[32];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(row_tmem + c * 32));
+      for (int c2 = 0; c2 < PAIR_N / 128; ++c2) {
+        // two 32-column loads in flight per wait
+        uint32_t r[64];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tmem_ld_32x32b_x32(row_tmem + (2 * c2 + h) * 32, r + 32 * h);
         tc_wait_ld();
-        if (c == PAIR_N / 64 - 1) {
+        tmem_ld_fence_regs<64>(r);
+        if (c2 == PAIR_N / 128 - 1) {
           // accumulator drained: hand it back to the MMA issuer of the pair
           tc_fence_before();
           __syncwarp();
@@ -432,25 +426,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           // a release would also wait for this row's global stores
           if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
         }
-        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha), __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
-        if (row_ok && c * 32 < cols) {
-          __nv_bfloat16* dst = orow + c * 32;
-          if (p.store32) {
-            // two 32-byte stores: each lane writes whole sectors (the
-            // scattered 16-byte form cost ~0.065 ms on the canonical case)
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * c2 + h;
+          uint32_t w[16];
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * h), "r"(w[8 * h]),
-                           "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
-                           "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
-                           : "memory");
-          } else {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+          for (int i = 0; i < 16; ++i)
+            w[i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[32 * h + 2 * i]), alpha),
+                             __fmul_rn(__uint_as_float(r[32 * h + 2 * i + 1]), alpha));
+          if (row_ok && c * 32 < cols) {
+            __nv_bfloat16* dst = orow + c * 32;
+            if (p.store32) {
+              // two 32-byte stores: each lane writes whole sectors (the
+              // scattered 16-byte form cost ~0.065 ms on the canonical case)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+              for (int k2 = 0; k2 < 2; ++k2)
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * k2), "r"(w[8 * k2]),
+                             "r"(w[8 * k2 + 1]), "r"(w[8 * k2 + 2]), "r"(w[8 * k2 + 3]), "r"(w[8 * k2 + 4]),
+                             "r"(w[8 * k2 + 5]), "r"(w[8 * k2 + 6]), "r"(w[8 * k2 + 7])
+                             : "memory");
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
           }
         }
       }
