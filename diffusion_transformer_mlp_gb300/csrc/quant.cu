@@ -29,9 +29,12 @@
 namespace nvfp4 {
 namespace {
 
-// SwiGLU kernels run one CTA of 1024 threads per SM with the whole silu table
-// (128 KB) in shared memory; weight kernels need no table.
-constexpr int kThreadsSwiglu = 1024;
+// SwiGLU kernels run one CTA per SM with the whole silu table (128 KB) in
+// shared memory: 1024 threads for pass 1, 768 for pass 2 (which keeps the
+// next unit's loads in registers while it computes, 80 registers a thread);
+// weight kernels need no table.
+constexpr int kThreadsAmaxSwiglu = 1024;
+constexpr int kThreadsQuantSwiglu = 768;
 constexpr int kThreadsWeight = 256;
 constexpr int kSegElems = 512;  // elements of one row handled by one warp per unit (16 per lane)
 constexpr int kTableBytes = 65536 * 2;
@@ -168,7 +171,7 @@ struct UnitWalker {
 // in flight per warp; loads keep the default L2 policy so the tail of the
 // tensor is still in L2 when pass 2 (which walks backwards) starts.
 template <bool kSwiglu>
-__global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
+__global__ void __launch_bounds__(kSwiglu ? kThreadsAmaxSwiglu : kThreadsWeight)
     k_amax(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, nvfp4_scale_rec* rec) {
   extern __shared__ __align__(16) uint16_t tab[];
   __shared__ uint32_t wmax[32];
@@ -217,6 +220,31 @@ __device__ __forceinline__ bool near_boundary(float q) {
   return ((__float_as_uint(q) + 3u) & mask) <= 6u;
 }
 
+// Two binary32 products RN(a*s), RN(b*s) in one packed multiply.
+__device__ __forceinline__ void mul2_rn(float a, float b, float s, float& x, float& y) {
+  asm("{\n\t.reg .b64 t, u, v;\n\t"
+      "mov.b64 t, {%2, %3};\n\t"
+      "mov.b64 u, {%4, %4};\n\t"
+      "mul.rn.f32x2 v, t, u;\n\t"
+      "mov.b64 {%0, %1}, v;\n\t}"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "f"(s));
+}
+
+// Eight E2M1 codes (RNE, satfinite) packed two per byte, q[0] in bits 0..3.
+__device__ __forceinline__ uint32_t e2m1x8_pack(const float* q) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return w;
+}
+
 // Block scale code of a block with max |h| = bmax: E4M3(RN(bmax / d)).
 __device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float rd) {
   if (d == 0.0f) return 0u;
@@ -229,7 +257,7 @@ __device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float 
 // [0, rows_pad), walked from the end so that the first reads hit what pass 1
 // left in L2; rows >= rows are zeros.
 template <bool kSwiglu>
-__global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
+__global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight)
     k_quant(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int64_t rows_pad,
             uint8_t* __restrict__ qdata, uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
   extern __shared__ __align__(16) uint16_t tab[];
@@ -251,24 +279,45 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
   const int64_t cpad4 = (cols / 16 + 3) / 4;  // 4-column scale groups per row
   const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
-  for (UnitWalker w(first, stride, segs); w.row < rows_pad; w.next()) {
-    const int64_t r = rows_pad - 1 - w.row;
-    const int64_t seg = segs - 1 - w.seg;
+  // Software pipeline: the loads of the next unit are issued before the
+  // current one is computed, so a warp keeps its loads in flight while it
+  // works (pass 2 is otherwise latency bound on them).
+  UnitWalker w(first, stride, segs);
+  int64_t r_n = rows_pad - 1 - w.row, seg_n = segs - 1 - w.seg;
+  bool more = w.row < rows_pad;
+  Slice s_n;
+  {
+    const int64_t c0 = seg_n * kSegElems + lane * 16;
+    if (more && c0 < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + r_n * ld, cols, c0, s_n);
+  }
+  while (more) {
+    const int64_t r = r_n, seg = seg_n;
     const int64_t c0 = seg * kSegElems + lane * 16;
     const bool valid = c0 < cols;
+    const bool loaded = valid && finite && r < rows;
+    const Slice s = s_n;
+    w.next();
+    more = w.row < rows_pad;
+    r_n = rows_pad - 1 - w.row;
+    seg_n = segs - 1 - w.seg;
+    {
+      const int64_t c0n = seg_n * kSegElems + lane * 16;
+      if (more && c0n < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + r_n * ld, cols, c0n, s_n);
+    }
     uint32_t hw[8];  // 16 BF16 values of h, two per word
-    if (valid && finite && r < rows) {
-      Slice s;
-      load_slice<kSwiglu, true>(x + r * ld, cols, c0, s);
+    if (loaded) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(s.g[i], s.u[i], tab) : s.g[i];
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) hw[i] = 0u;
     }
-    uint32_t m2 = 0;
+    // |h| max per half; no NaN reaches here (a NaN or Inf anywhere makes the
+    // global max non-finite, and then no element is read)
+    __nv_bfloat162 mh = __floats2bfloat162_rn(0.0f, 0.0f);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m2 = max_pair(m2, hw[i] & 0x7FFF7FFFu);
+    for (int i = 0; i < 8; ++i) mh = __hmax2(mh, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&hw[i])));
+    const uint32_t m2 = *reinterpret_cast<const uint32_t*>(&mh);
     const float bmax = __uint_as_float(max((m2 << 16) & 0x7FFFFFFFu, m2 & 0x7FFF0000u));
     const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
     const float sc = __fmul_rn(e4m3_value(bs), g);
@@ -276,25 +325,20 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
     if (sc != 0.0f && finite) {
       const float rs = __frcp_rn(sc);
       float q[16];
-      bool near = false;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        q[2 * i] = __fmul_rn(bf16_to_f32(hw[i] & 0xFFFFu), rs);
-        q[2 * i + 1] = __fmul_rn(__uint_as_float(hw[i] & 0xFFFF0000u), rs);
-        near |= near_boundary<3>(q[2 * i]) | near_boundary<3>(q[2 * i + 1]);
-      }
-      if (near) {
+      for (int i = 0; i < 8; ++i)
+        mul2_rn(bf16_to_f32(hw[i] & 0xFFFFu), __uint_as_float(hw[i] & 0xFFFF0000u), rs, q[2 * i], q[2 * i + 1]);
+      // Only the quotients near a rounding boundary are recomputed by a true
+      // division.  With h and the global max both BF16 and 2688 = 2^7 * 21,
+      // h / sc is a ratio of small integers and lands on or next to a
+      // 3-significant-bit number often enough that redoing whole blocks kept
+      // the division path busy in most warps.
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          q[2 * i] = __fdiv_rn(bf16_to_f32(hw[i] & 0xFFFFu), sc);
-          q[2 * i + 1] = __fdiv_rn(__uint_as_float(hw[i] & 0xFFFF0000u), sc);
-        }
-      }
-      uint32_t b[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) b[i] = e2m1x2_code(q[2 * i], q[2 * i + 1]);
-      packed.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-      packed.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+      for (int j = 0; j < 16; ++j)
+        if (near_boundary<3>(q[j]))
+          q[j] = __fdiv_rn((j & 1) ? __uint_as_float(hw[j >> 1] & 0xFFFF0000u) : bf16_to_f32(hw[j >> 1] & 0xFFFFu), sc);
+      packed.x = e2m1x8_pack(q);
+      packed.y = e2m1x8_pack(q + 8);
     }
     if (valid) *reinterpret_cast<uint2*>(qdata + r * (cols / 2) + c0 / 2) = packed;
 
@@ -311,8 +355,8 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsSwiglu : kThreadsWeight)
 }
 
 template <typename K>
-nvfp4_status launch_stream_kernel(K kernel, bool swiglu, cudaStream_t stream, const char* name, auto... args) {
-  const int threads = swiglu ? kThreadsSwiglu : kThreadsWeight;
+nvfp4_status launch_stream_kernel(K kernel, bool swiglu, int threads, cudaStream_t stream, const char* name,
+                                  auto... args) {
   const int smem = swiglu ? kTableBytes : 0;
   nvfp4_status st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem), name);
   if (st != NVFP4_OK) return st;
@@ -342,13 +386,13 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
   nvfp4_status st = cuda_check(cudaMemsetAsync(rec, 0, sizeof(nvfp4_scale_rec), stream), "memset rec");
   if (st != NVFP4_OK) return st;
   if (swiglu) {
-    if ((st = launch_stream_kernel(k_amax<true>, true, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
+    if ((st = launch_stream_kernel(k_amax<true>, true, kThreadsAmaxSwiglu, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
       return st;
-    return launch_stream_kernel(k_quant<true>, true, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
+    return launch_stream_kernel(k_quant<true>, true, kThreadsQuantSwiglu, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
   }
-  if ((st = launch_stream_kernel(k_amax<false>, false, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
+  if ((st = launch_stream_kernel(k_amax<false>, false, kThreadsWeight, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
     return st;
-  return launch_stream_kernel(k_quant<false>, false, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
+  return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
 }
 
 // ---- diagnostics: the same device functions on test-chosen inputs ----------
