@@ -154,10 +154,15 @@ def fc2(gate_up: torch.Tensor, w: NVFP4Tensor, act: NVFP4Tensor | None = None, o
 
 
 def fc2_host(gate_up_host: torch.Tensor, w: NVFP4Tensor, workspace: dict | None = None, stream=None,
-             out_host: torch.Tensor | None = None) -> torch.Tensor:
+             out_host: torch.Tensor | None = None, sync: bool = True):
     """FC2 from host memory to host memory: copy gate|up to the device, run
     the step, copy the BF16 output back.  Pinned host tensors make the copies
-    asynchronous; `workspace` (a dict) keeps device buffers between calls."""
+    asynchronous; `workspace` (a dict) keeps device buffers between calls.
+
+    With ``sync=False`` the call returns ``(out_host, event)`` as soon as the
+    work is queued on `stream`; `out_host` is valid, and `workspace` and
+    `gate_up_host` may be reused, once `event` has completed.  Two workspaces
+    on two streams let one step's copies overlap another step's kernels."""
     m, two_k = gate_up_host.shape
     k = two_k // 2
     ws = workspace if workspace is not None else {}
@@ -176,5 +181,9 @@ def fc2_host(gate_up_host: torch.Tensor, w: NVFP4Tensor, workspace: dict | None 
         if out_host is None:
             out_host = torch.empty(m, w.rows, dtype=torch.bfloat16, pin_memory=True)
         out_host.copy_(ws["out"], non_blocking=True)
-    s.synchronize()
-    return out_host
+    if sync:
+        s.synchronize()
+        return out_host
+    ev = torch.cuda.Event()
+    ev.record(s)
+    return out_host, ev

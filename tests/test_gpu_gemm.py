@@ -123,3 +123,30 @@ def test_gemm_row_invariance_across_m(canonical):
         out = fc2.nvfp4_fc2_gemm(a_m, w_dev)
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), base[:m].view(torch.int16)), m
+
+
+def test_fc2_host_matches_device_step():
+    """fc2_host (pinned host gate|up in, host BF16 out), synchronous and
+    queued on two streams with two workspaces, gives the bytes of the
+    device-side step."""
+    m, n, k = 300, 256, 1024
+    x = synth.activation(m, k, seed=11)
+    w = synth.weight(n, k, seed=11)
+    wq = fc2.nvfp4_quantize_weight(to_dev_bf16(w))
+    ref = fc2.fc2(to_dev_bf16(x), wq)
+    torch.cuda.synchronize()
+    x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    got = fc2.fc2_host(x_host, wq)
+    assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [{}, {}]
+    outs = [torch.empty(m, n, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    evs = [None, None]
+    for i in range(6):
+        j = i % 2
+        if evs[j] is not None:
+            evs[j].synchronize()
+        _, evs[j] = fc2.fc2_host(x_host, wq, wss[j], streams[j], outs[j], sync=False)
+    for j in range(2):
+        evs[j].synchronize()
+        assert torch.equal(outs[j].view(torch.int16), ref.cpu().view(torch.int16))
