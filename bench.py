@@ -331,6 +331,23 @@ def run_ours(args):
         e2e_step(i)
     for sl in slots:
         sl["ev"].synchronize()
+    # The host link these copies run on, measured on the same buffers (it
+    # differs between machines, e.g. with the NUMA placement of pinned memory).
+    link = {}
+    if e2e_steps:
+        sl = slots[0]
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(sl["stream"]):
+            c0.record(sl["stream"])
+            sl["ws"]["x"].copy_(x_host, non_blocking=True)
+            c1.record(sl["stream"])
+            c1.synchronize()
+            link["h2d_gbs"] = x_host.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
+            c0.record(sl["stream"])
+            sl["out"].copy_(sl["ws"]["out"], non_blocking=True)
+            c1.record(sl["stream"])
+            c1.synchronize()
+            link["d2h_gbs"] = M * N * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     barrier()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
@@ -341,7 +358,7 @@ def run_ours(args):
     e2e_s = max_over_ranks(e2e_s, dev)
     e2e = {"value": job_throughput(world, FLOP, e2e_s), "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": M * N * 2,
-           "steps": e2e_steps,
+           "steps": e2e_steps, "host_link_measured": link,
            "api": "nvfp4_quantize_weight + fc2_host(sync=False), two slots (pinned host gate|up in, host BF16 out)"}
 
     # ---- roofline of the dominant kernel
