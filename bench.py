@@ -37,6 +37,9 @@ WORKLOAD = "canonical FC2: gate|up bf16 [37810, 2x14336] N(0,1)+0.1% x20 -> SwiG
 # Scheduling Results", Timing): 38.823 ms -> 2MNK / 38.823 ms.
 PAGES_STEP_MS = 38.823
 PAGES_TFLOPS = 2 * M * N * K / (PAGES_STEP_MS * 1e-3) / 1e12
+# NVIDIA's published dense (non-sparse) FP4 tensor throughput of one GB300
+# GPU: 1,080 PFLOP/s dense FP4 for the 72 GPUs of a GB300 NVL72 rack.
+NVIDIA_DENSE_FP4_TFLOPS = 15000.0
 
 
 def producer_bytes(m, k):
@@ -219,6 +222,53 @@ def traffic_record(kernel: str):
     return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
 
 
+def fp4_mma_loop(dev, uuid, seconds: float = 1.0, iters: int = 65536):
+    """Dense NVFP4 tensor-core throughput measured in-repo: the shared-memory
+    resident tcgen05 mxf4nvf4 loop of nvfp4_diag_mma_peak, launched back to
+    back for about `seconds` so that the clocks settle under the power cap.
+    `burst` is the fastest launch, `sustained` the mean of the second half."""
+    import ctypes
+
+    import torch
+
+    from diffusion_transformer_mlp_gb300 import _lib
+
+    L = _lib.load()
+    pairs = int(L.nvfp4_diag_mma_peak_pairs())
+    if pairs < 1:
+        return None
+    flop = pairs * iters * 2 * 256 * 256 * 64
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp, stp = ctypes.c_void_p(stream.cuda_stream), ctypes.c_void_p(st.data_ptr())
+    _lib.check(L.nvfp4_diag_mma_peak(iters, stp, sp), "nvfp4_diag_mma_peak")
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    _lib.check(L.nvfp4_diag_mma_peak(iters, stp, sp), "nvfp4_diag_mma_peak")
+    c1.record(stream)
+    torch.cuda.synchronize()
+    n = max(4, min(400, int(seconds / max(c0.elapsed_time(c1) * 1e-3, 1e-4))))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.2)
+    evs[0].record(stream)
+    for i in range(n):
+        _lib.check(L.nvfp4_diag_mma_peak(iters, stp, sp), "nvfp4_diag_mma_peak")
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if int(st.item()) != 0:
+        raise RuntimeError("FP4 MMA loop reported a device timeout")
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    tf = [flop / (t * 1e-3) / 1e12 for t in ms]
+    return {"burst_tflops": max(tf), "sustained_tflops": statistics.mean(tf[n // 2:]), "pairs": pairs,
+            "iters_per_launch": iters, "launches": n, "flop_per_launch": flop,
+            "ms_per_launch_mean": statistics.mean(ms), "clocks": clocks,
+            "kernel": "k_diag_mma_peak (tcgen05.mma.cta_group::2.kind::mxf4nvf4 M256 N256 K64, smem operands)"}
+
+
 def run_ours(args):
     global M
     if args.m is not None:
@@ -364,12 +414,16 @@ def run_ours(args):
     # ---- roofline of the dominant kernel
     gemm_tflops = FLOP / (gemm_ms * 1e-3) / 1e12
     fp4_peak = peaks["bf16_tflops"] * 6.0  # dense FP4 / BF16 nominal ratio 13.5 / 2.25
+    loop = None if args.no_mma_loop else fp4_mma_loop(dev, uuid)
     pbytes = producer_bytes(M, K)
     if not e2e_steps:
         e2e = None
     prod_gbs = pbytes / (prod_ms * 1e-3) / 1e9
     kernels = {
-        "gemm": {"ms": gemm_ms, "tflops": gemm_tflops, "frac_of_fp4_peak": gemm_tflops / fp4_peak},
+        "gemm": {"ms": gemm_ms, "tflops": gemm_tflops, "frac_of_fp4_peak": gemm_tflops / fp4_peak,
+                 "fp4_mma_loop": loop,
+                 "frac_of_fp4_mma_loop_burst": gemm_tflops / loop["burst_tflops"] if loop else None,
+                 "nvidia_published_dense_fp4_tflops": NVIDIA_DENSE_FP4_TFLOPS},
         "swiglu_producer": {"ms": prod_ms, "algorithmic_bytes": pbytes, "gbs": prod_gbs,
                             "frac_of_hbm": prod_gbs / peaks["hbm_gbs"],
                             "one_read_bytes": M * 2 * K * 2 + fc2.qdata_bytes(M, K) + fc2.scale_bytes(M, K)},
@@ -415,6 +469,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-mma-loop", action="store_true", help="skip the in-repo dense FP4 tensor-core loop")
     ap.add_argument("--m", type=int, default=None,
                     help="override M (smaller cases for ncu captures; not a bench line)")
     args = ap.parse_args()

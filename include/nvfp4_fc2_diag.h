@@ -47,6 +47,24 @@ nvfp4_status nvfp4_diag_code_transitions(int which, uint32_t* trans, uint32_t ca
 nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status,
                                      nvfp4_stream_t stream);
 
+/* Dense NVFP4 tensor-core throughput of this GPU, the denominator of the
+ * GEMM's roofline ("FC2 NVFP4 Scheduling Results", Canonical Operation: the
+ * FC2 is a dense E2M1 x E2M1 contraction with UE4M3 vector-16 scales).
+ * P SM pairs (nvfp4_diag_mma_peak_pairs()) each run `iters` back-to-back
+ * tcgen05.mma.cta_group::2.kind::mxf4nvf4 (M=256, N=256, K=64, i.e.
+ * 2*256*256*64 = 8388608 FLOP each) on operands resident in shared memory
+ * (fixed pseudo-random bytes, all scales 1.0) with nothing else on the
+ * tensor pipe.  The caller times the launch on `stream`: FLOP per launch =
+ * P * iters * 8388608.  1 <= iters <= 2^22, else NVFP4_EINVAL.  If the
+ * final bounded wait runs out, NVFP4_ETIMEOUT is written to *dev_status
+ * (device uint32; may be NULL); the accumulators are discarded. */
+nvfp4_status nvfp4_diag_mma_peak(int64_t iters, uint32_t* dev_status, nvfp4_stream_t stream);
+
+/* P above: the SM pairs that hold one two-CTA cluster of the loop each at
+ * the same time on the current device (SMs / 2 unless fewer fit); -1 if
+ * the CUDA query fails. */
+int64_t nvfp4_diag_mma_peak_pairs(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -106,6 +106,8 @@ def test_diag_argument_errors():
     assert L.nvfp4_diag_code_transitions(2, P16, 10, P16, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_wait_timeout(0, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_wait_timeout(10 ** 10, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_mma_peak(0, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_mma_peak((1 << 22) + 1, P16, NUL) == _lib.NVFP4_EINVAL
 
 
 def test_product_package_does_not_import_oracle():

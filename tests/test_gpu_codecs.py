@@ -110,3 +110,27 @@ def test_bounded_wait_reports_timeout_without_hanging():
     # the context is still usable
     x = torch.ones(4, device="cuda")
     assert float((x + 1).sum().item()) == 8.0
+
+
+def test_fp4_mma_loop_runs_and_scales():
+    """The dense FP4 tensor-core loop ends without a timeout, its time grows
+    in proportion to the MMAs issued, and its rate lies between the BF16
+    nominal peak (a dense FP4 rate below it means the loop is not running on
+    the FP4 path) and twice NVIDIA's dense FP4 figure for the part."""
+    L = _lib.load()
+    pairs = int(L.nvfp4_diag_mma_peak_pairs())
+    assert 1 <= pairs <= torch.cuda.get_device_properties(0).multi_processor_count // 2
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ms = {}
+    for iters in (4096, 4096, 65536):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        _lib.check(L.nvfp4_diag_mma_peak(iters, _p(st), _stream()), "mma loop")
+        c1.record()
+        torch.cuda.synchronize()
+        ms[iters] = c0.elapsed_time(c1)
+    assert int(st.item()) == 0
+    ratio = ms[65536] / ms[4096]
+    assert 8.0 < ratio < 20.0, ms
+    tflops = pairs * 65536 * 2 * 256 * 256 * 64 / (ms[65536] * 1e-3) / 1e12
+    assert 2250.0 < tflops < 30000.0, tflops
