@@ -88,9 +88,9 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;  // 256 FP32 columns
 // Block scales in tensor memory, two slots used by alternate stages
 // (KSTEPS K=64 steps j each):
-//   A: step j at column slot + 4j; the scales of accumulator row i are read
-//      from lane i, column slot + 4j + i/32 (the word is stored in all four
-//      columns).
+//   A: step j at columns slot + 4j .. + 3; the scales of accumulator row i
+//      are read from lane i, column slot + 4j + i/32, and only that column
+//      is written.
 //   W: step j at column slot + SFW_COL + 8j; accumulator rows of lane
 //      quarter g read the scales of W row n from lane 32g + n % 32, column
 //      slot + SFW_COL + 8j + n/32, so every quarter holds a copy.
@@ -217,13 +217,12 @@ __device__ __forceinline__ void read_scales(ScaleWords& v, const uint8_t* slot, 
   }
 }
 
-__device__ __forceinline__ void store_scales(uint32_t taddr, const ScaleWords& v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%1,%1,%1,%2,%2,%2,%2,%3,%3,%3,%3,%4,%4,%4,%4,"
-      "%5,%5,%5,%5,%6,%6,%6,%6,%7,%7,%7,%7,%8,%8,%8,%8};" ::"r"(taddr),
-      "r"(v.a[0]), "r"(v.a[1]), "r"(v.a[2]), "r"(v.a[3]), "r"(v.a[4]), "r"(v.a[5]), "r"(v.a[6]), "r"(v.a[7])
-      : "memory");
+// A: a lane of quarter q reads only column 4j + q of step j, so the writer
+// of quarter q stores its word there alone (one column per step).
+__device__ __forceinline__ void store_scales(uint32_t taddr, const ScaleWords& v, int q) {
+#pragma unroll
+  for (int j = 0; j < KSTEPS; ++j)
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr + 4 * j + q), "r"(v.a[j]) : "memory");
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const uint4* x = v.w + 8 * half;
@@ -488,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         back.next(STAGES);
       }
       tc_fence_after();
-      store_scales(tmem + lane_base + SF_COL + uint32_t(sf_slot) * SF_SLOT_COLS, v);
+      store_scales(tmem + lane_base + SF_COL + uint32_t(sf_slot) * SF_SLOT_COLS, v, q);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
