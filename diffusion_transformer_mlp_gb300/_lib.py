@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_EINVAL", 2: "NVFP4_EUNSUPPORTED", 3: "N
 EXPORTED = ["nvfp4_padded_rows", "nvfp4_qdata_bytes", "nvfp4_scale_bytes", "nvfp4_scale_offset",
             "nvfp4_quantize_weight", "swiglu_nvfp4_quantize", "nvfp4_fc2_gemm", "nvfp4_last_error",
             "nvfp4_version", "nvfp4_diag_silu_all", "nvfp4_diag_swiglu", "nvfp4_diag_code_transitions",
-            "nvfp4_diag_wait_timeout", "nvfp4_diag_mma_peak", "nvfp4_diag_mma_peak_pairs"]
+            "nvfp4_diag_wait_timeout", "nvfp4_diag_mma_peak", "nvfp4_diag_mma_peak_pairs",
+            "nvfp4_diag_quotient_codes"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +84,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.nvfp4_diag_mma_peak.argtypes = [i64, vp, vp]
         L.nvfp4_diag_mma_peak_pairs.restype = i64
         L.nvfp4_diag_mma_peak_pairs.argtypes = []
+        L.nvfp4_diag_quotient_codes.restype = st
+        L.nvfp4_diag_quotient_codes.argtypes = [u32, u32, vp, vp]
         _lib = L
         return _lib
 

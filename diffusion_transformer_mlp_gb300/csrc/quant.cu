@@ -231,6 +231,19 @@ __device__ __forceinline__ void mul2_rn(float a, float b, float s, float& x, flo
       : "f"(a), "f"(b), "f"(s));
 }
 
+// Two binary32 fused multiply-adds RN(a*b + c) in one packed instruction.
+__device__ __forceinline__ void fma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& x,
+                                        float& y) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(x), "=f"(y)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // Eight E2M1 codes (RNE, satfinite) packed two per byte, q[0] in bits 0..3.
 __device__ __forceinline__ uint32_t e2m1x8_pack(const float* q) {
   uint32_t w;
@@ -243,6 +256,42 @@ __device__ __forceinline__ uint32_t e2m1x8_pack(const float* q) {
       : "=r"(w)
       : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
   return w;
+}
+
+// The 16 E2M1 codes of one block, packed two per byte (element 0 in bits
+// 0..3 of .x): E2M1(RN(h / sc)) for the 16 BF16 values in hw (two per word),
+// sc > 0 the block's decoded scale and rs = RN(1 / sc).
+// n = RN(h * -rs) = -RN(h * rs) is corrected once, Markstein's step (IBM J.
+// Res. Dev. 34, 1990): the residual r = h + n*sc is exact as one fma, and
+// RN(n + r*(-rs)) = -RN(q + r*rs) then rounds like -h / sc wherever an E2M1
+// code can change.  Working on -q keeps the sign of a zero h (+0 and -0 give
+// codes 0 and 8); the sign bits of the packed codes are flipped at the end.
+// Blocks with a scale below 2^-100 (a global max below ~1e-27) keep the
+// plain product and divide the quotients within 3 ulps of a
+// 3-significant-bit number, which also catches an infinite reciprocal.
+// Over every BF16 h, block-scale code and BF16 global max the codes equal
+// those of the correctly rounded quotient (nvfp4_diag_quotient_codes).
+__device__ __forceinline__ uint2 block_codes(const uint32_t* hw, float sc, float rs) {
+  const float nrs = -rs;
+  float n[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mul2_rn(bf16_to_f32(hw[i] & 0xFFFFu), __uint_as_float(hw[i] & 0xFFFF0000u), nrs, n[2 * i], n[2 * i + 1]);
+  if (sc >= 0x1p-100f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float r0, r1;
+      fma2_rn(n[2 * i], n[2 * i + 1], sc, sc, bf16_to_f32(hw[i] & 0xFFFFu), __uint_as_float(hw[i] & 0xFFFF0000u),
+              r0, r1);
+      fma2_rn(r0, r1, nrs, nrs, n[2 * i], n[2 * i + 1], n[2 * i], n[2 * i + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (near_boundary<3>(n[j]))
+        n[j] = __fdiv_rn((j & 1) ? __uint_as_float(hw[j >> 1] & 0xFFFF0000u) : bf16_to_f32(hw[j >> 1] & 0xFFFFu), -sc);
+  }
+  return make_uint2(e2m1x8_pack(n) ^ 0x88888888u, e2m1x8_pack(n + 8) ^ 0x88888888u);
 }
 
 // Block scale code of a block with max |h| = bmax: E4M3(RN(bmax / d)).
@@ -322,24 +371,7 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
     const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
     const float sc = __fmul_rn(e4m3_value(bs), g);
     uint2 packed = make_uint2(0u, 0u);
-    if (sc != 0.0f && finite) {
-      const float rs = __frcp_rn(sc);
-      float q[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        mul2_rn(bf16_to_f32(hw[i] & 0xFFFFu), __uint_as_float(hw[i] & 0xFFFF0000u), rs, q[2 * i], q[2 * i + 1]);
-      // Only the quotients near a rounding boundary are recomputed by a true
-      // division.  With h and the global max both BF16 and 2688 = 2^7 * 21,
-      // h / sc is a ratio of small integers and lands on or next to a
-      // 3-significant-bit number often enough that redoing whole blocks kept
-      // the division path busy in most warps.
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (near_boundary<3>(q[j]))
-          q[j] = __fdiv_rn((j & 1) ? __uint_as_float(hw[j >> 1] & 0xFFFF0000u) : bf16_to_f32(hw[j >> 1] & 0xFFFFu), sc);
-      packed.x = e2m1x8_pack(q);
-      packed.y = e2m1x8_pack(q + 8);
-    }
+    if (sc != 0.0f && finite) packed = block_codes(hw, sc, __frcp_rn(sc));
     if (valid) *reinterpret_cast<uint2*>(qdata + r * (cols / 2) + c0 / 2) = packed;
 
     // scales: lanes 4j..4j+3 hold the four blocks of scale group j
@@ -468,6 +500,49 @@ __global__ void k_diag_transitions(int which, uint32_t* trans, uint32_t cap, uin
   }
 }
 
+// Every (global max, block-scale code, h) through block_codes, against the
+// definition E2M1(RN(h / sc)) with RN(h / sc) from the correctly rounded
+// division.  Global maxima A are the BF16 patterns a_first .. a_first +
+// a_count - 1 (g = RN(A / 2688), as pass 2 forms it), block-scale codes
+// 1..126 (sc = RN(E4M3(bs) * g), blocks with sc = 0 are never encoded), and
+// every BF16 h of either sign with |h| <= A (a block's values never exceed
+// the global max), 16 to a block.
+// counts[0] += codes that differ, counts[1] += codes compared.
+__global__ void k_diag_quotient_codes(uint32_t a_first, uint32_t a_count, unsigned long long* counts) {
+  constexpr uint32_t kFinite = 0x7F80u;            // non-negative finite BF16 patterns
+  constexpr uint32_t kChunks = 2 * kFinite / 16;  // blocks of 16 values, both signs
+  unsigned long long bad = 0, seen = 0;
+  const uint64_t items = uint64_t(a_count) * 126u * kChunks;
+  for (uint64_t it = blockIdx.x * uint64_t(blockDim.x) + threadIdx.x; it < items;
+       it += uint64_t(gridDim.x) * blockDim.x) {
+    const uint32_t chunk = uint32_t(it % kChunks);
+    const uint32_t bs = 1u + uint32_t((it / kChunks) % 126u);
+    const uint32_t abits = a_first + uint32_t(it / (uint64_t(kChunks) * 126u));
+    const float g = __fdiv_rn(bf16_to_f32(abits), 2688.0f);
+    const float sc = __fmul_rn(e4m3_value(bs), g);
+    if (!(sc > 0.0f)) continue;
+    uint32_t hb[16], hw[8];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t k = chunk * 16u + uint32_t(j);
+      hb[j] = k < kFinite ? k : 0x8000u + (k - kFinite);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hw[i] = hb[2 * i] | (hb[2 * i + 1] << 16);
+    const uint2 c = block_codes(hw, sc, __frcp_rn(sc));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if ((hb[j] & 0x7FFFu) > abits) continue;
+      const uint32_t got = ((j < 8 ? c.x : c.y) >> (4 * (j & 7))) & 0xFu;
+      const uint32_t want = e2m1x2_code(__fdiv_rn(bf16_to_f32(hb[j]), sc), 0.0f) & 0xFu;
+      bad += got != want ? 1u : 0u;
+      ++seen;
+    }
+  }
+  atomicAdd(&counts[0], bad);
+  atomicAdd(&counts[1], seen);
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -513,4 +588,13 @@ extern "C" nvfp4_status nvfp4_diag_code_transitions(int which, uint32_t* trans, 
   k_diag_transitions<<<sm_count() * 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(which, trans, cap, count,
                                                                                           first_code);
   return cuda_check(cudaGetLastError(), "launch k_diag_transitions");
+}
+
+extern "C" nvfp4_status nvfp4_diag_quotient_codes(uint32_t a_first, uint32_t a_count, uint64_t* counts,
+                                                  nvfp4_stream_t stream) {
+  if (!counts || a_count < 1 || a_first >= 0x7F80u || a_count > 0x7F80u - a_first)
+    return fail(NVFP4_EINVAL, "nvfp4_diag_quotient_codes: bad arguments");
+  k_diag_quotient_codes<<<sm_count() * 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      a_first, a_count, reinterpret_cast<unsigned long long*>(counts));
+  return cuda_check(cudaGetLastError(), "launch k_diag_quotient_codes");
 }

@@ -47,6 +47,21 @@ nvfp4_status nvfp4_diag_code_transitions(int which, uint32_t* trans, uint32_t ca
 nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status,
                                      nvfp4_stream_t stream);
 
+/* The element encoder of pass 2 (h -> E2M1 code of h / sc), swept against
+ * its definition ("FC2 NVFP4 Scheduling Results", Canonical Operation: E2M1
+ * elements of h divided by the decoded block scale): for every global max
+ * A among the BF16 patterns a_first .. a_first + a_count - 1 (g =
+ * RN(A / 2688)), every block-scale code 1..126 with sc = RN(E4M3 * g) > 0,
+ * and every BF16 h of either sign with |h| <= A (the values of a block never
+ * exceed the global max), the producer's code is compared
+ * with E2M1(RN(h / sc)), RN(h / sc) the correctly rounded division.
+ * counts (device, two uint64, zeroed by the caller) receives += {codes that
+ * differ, codes compared}.  a_first + a_count <= 0x7F80 (finite maxima),
+ * a_count >= 1, else NVFP4_EINVAL.  All 32,639 nonzero maxima take a few
+ * seconds in total. */
+nvfp4_status nvfp4_diag_quotient_codes(uint32_t a_first, uint32_t a_count, uint64_t* counts,
+                                       nvfp4_stream_t stream);
+
 /* Dense NVFP4 tensor-core throughput of this GPU, the denominator of the
  * GEMM's roofline ("FC2 NVFP4 Scheduling Results", Canonical Operation: the
  * FC2 is a dense E2M1 x E2M1 contraction with UE4M3 vector-16 scales).

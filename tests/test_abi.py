@@ -107,6 +107,10 @@ def test_diag_argument_errors():
     assert L.nvfp4_diag_wait_timeout(0, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_wait_timeout(10 ** 10, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_mma_peak(0, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_quotient_codes(1, 0, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_quotient_codes(0x7F80, 1, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_quotient_codes(1, 0x7F80, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_quotient_codes(1, 1, NUL, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_mma_peak((1 << 22) + 1, P16, NUL) == _lib.NVFP4_EINVAL
 
 

@@ -134,3 +134,33 @@ def test_fp4_mma_loop_runs_and_scales():
     assert 8.0 < ratio < 20.0, ms
     tflops = pairs * 65536 * 2 * 256 * 256 * 64 / (ms[65536] * 1e-3) / 1e12
     assert 2250.0 < tflops < 30000.0, tflops
+
+
+def _e4m3_values():
+    """UE4M3 values of codes 1..126: subnormals m * 2^-9, normals (1 + m/8) * 2^(e-7)."""
+    c = np.arange(1, 127)
+    e, m = c >> 3, c & 7
+    return np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * 2.0 ** (e - 7)).astype(np.float32)
+
+
+def test_element_codes_match_correctly_rounded_quotient_everywhere():
+    """Pass 2's element encoder (a multiply by the reciprocal with one fma
+    correction step) gives E2M1(RN(h / sc)) for every BF16 global max A, every
+    block-scale code and every BF16 h with |h| <= A, both signs (1.3e11 codes)."""
+    L = _lib.load()
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    first, last = 1, 0x7F7F
+    a = first
+    while a <= last:
+        n = min(2048, last - a + 1)
+        _lib.check(L.nvfp4_diag_quotient_codes(a, n, _p(counts), _stream()), "quotient codes")
+        a += n
+    torch.cuda.synchronize()
+    bad, seen = (int(v) for v in counts.cpu())
+    # codes compared: the 2 (A + 1) patterns h with |h| <= A, per (max A,
+    # scale) pair whose scale is nonzero
+    abits = np.arange(first, last + 1, dtype=np.uint32)
+    g = (abits << 16).view(np.float32) / np.float32(2688.0)
+    sc = _e4m3_values()[None, :] * g[:, None]
+    assert seen == int(((sc > 0).sum(axis=1) * 2 * (abits.astype(np.int64) + 1)).sum())
+    assert bad == 0
