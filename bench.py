@@ -269,6 +269,62 @@ def fp4_mma_loop(dev, uuid, seconds: float = 1.0, iters: int = 65536):
             "kernel": "k_diag_mma_peak (tcgen05.mma.cta_group::2.kind::mxf4nvf4 M256 N256 K64, smem operands)"}
 
 
+def fc1_and_chain(dev, x, wq2, act2, out2, fp4_peak, loop, reps: int = 20):
+    """FC1 on the same kernel (M x 2*14336 x 5376) and the block's chain
+    FC1 -> SwiGLU producer -> FC2 with both weights already in NVFP4.  FC1's
+    input stands in for the modulated hidden state (not on the pages): BF16
+    [M, 5376] of the activation law, quantised by the plain NVFP4 quantiser.
+    FC1 writes its [M, 28672] output into the gate|up buffer `x`, which the
+    producer then reads: the chain runs on FC1's own output."""
+    import numpy as np
+    import torch
+
+    import diffusion_transformer_mlp_gb300 as fc2
+    import synth
+
+    n1, k1 = 2 * K, N
+    h_host = synth.quant_input(M, k1, seed=1)
+    w1_host = synth.weight(n1, k1, seed=1)
+    h = torch.from_numpy(h_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    w1 = torch.from_numpy(w1_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    act1 = fc2.nvfp4_quantize_weight(h)
+    wq1 = fc2.nvfp4_quantize_weight(w1)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    fc1_ms = timed(lambda: fc2.nvfp4_fc2_gemm(act1, wq1, x, status, stream))
+
+    def chain():
+        fc2.nvfp4_fc2_gemm(act1, wq1, x, status, stream)
+        fc2.swiglu_nvfp4_quantize(x, act2, stream)
+        fc2.nvfp4_fc2_gemm(act2, wq2, out2, status, stream)
+
+    chain_ms = timed(chain)
+    if int(status.item()) != 0 or fc2.read_rec(act2)["status"] != 0:
+        raise RuntimeError("device status not OK in the FC1 / chain measurement")
+    fc1_flop = 2 * M * n1 * k1
+    fc1_tflops = fc1_flop / (fc1_ms * 1e-3) / 1e12
+    chain_flop = fc1_flop + 2 * M * N * K
+    return {"fc1_gemm": {"shape": [M, n1, k1], "ms": fc1_ms, "tflops": fc1_tflops,
+                         "frac_of_fp4_peak": fc1_tflops / fp4_peak,
+                         "frac_of_fp4_mma_loop_burst": fc1_tflops / loop["burst_tflops"] if loop else None,
+                         "input": "BF16 [M, 5376] of the activation law (stand-in for the modulated hidden state), plain NVFP4"},
+            "mlp_chain": {"ms": chain_ms, "tflops": chain_flop / (chain_ms * 1e-3) / 1e12,
+                          "steps": "FC1 GEMM -> SwiGLU producer on FC1's output -> FC2 GEMM; weights pre-quantised"}}
+
+
 def run_ours(args):
     global M
     if args.m is not None:
@@ -415,6 +471,7 @@ def run_ours(args):
     gemm_tflops = FLOP / (gemm_ms * 1e-3) / 1e12
     fp4_peak = peaks["bf16_tflops"] * 6.0  # dense FP4 / BF16 nominal ratio 13.5 / 2.25
     loop = None if args.no_mma_loop else fp4_mma_loop(dev, uuid)
+    extra = None if args.no_fc1 else fc1_and_chain(dev, x, wq, act, out, fp4_peak, loop)
     pbytes = producer_bytes(M, K)
     if not e2e_steps:
         e2e = None
@@ -429,6 +486,8 @@ def run_ours(args):
                             "one_read_bytes": M * 2 * K * 2 + fc2.qdata_bytes(M, K) + fc2.scale_bytes(M, K)},
         "weight_quant": {"ms": wq_ms},
     }
+    if extra:
+        kernels.update(extra)
     if gemm_ms >= prod_ms:
         roofline = {"kernel": "k_fc2_gemm", "bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak,
                     "unit": "TFLOP/s", "frac": gemm_tflops / fp4_peak, "traffic": traffic_record("k_fc2_gemm"),
@@ -470,6 +529,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-mma-loop", action="store_true", help="skip the in-repo dense FP4 tensor-core loop")
+    ap.add_argument("--no-fc1", action="store_true", help="skip the FC1 GEMM and FC1 -> producer -> FC2 chain")
     ap.add_argument("--m", type=int, default=None,
                     help="override M (smaller cases for ncu captures; not a bench line)")
     args = ap.parse_args()

@@ -150,3 +150,43 @@ def test_fc2_host_matches_device_step():
     for j in range(2):
         evs[j].synchronize()
         assert torch.equal(outs[j].view(torch.int16), ref.cpu().view(torch.int16))
+
+
+# FC1 on the same kernel: M x (2 * 14336) x 5376.  Its input is the block's
+# modulated hidden state, whose modulation is not on the pages; here it is a
+# BF16 [M, 5376] matrix of the activation law, quantised to NVFP4 by the
+# plain (non-SwiGLU) quantiser.  K = 5376 is 21 k-tiles: an odd count.
+FC1_N, FC1_K = 2 * 14336, 5376
+
+
+def build_fc1_case(m, seed):
+    x = synth.quant_input(m, FC1_K, seed=seed)
+    w = synth.weight(FC1_N, FC1_K, seed=seed)
+    a_ref = oracle.quantize(x, FC1_K, swiglu=False)
+    w_ref = oracle.quantize(w, FC1_K, swiglu=False)
+    a_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(x))
+    w_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(w))
+    return a_ref, w_ref, a_dev, w_dev
+
+
+def test_fc1_all_rows():
+    """FC1 shape, M = 300 (a ragged 256-row tile): every output element."""
+    m = 300
+    a_ref, w_ref, a_dev, w_dev = build_fc1_case(m, seed=11)
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, np.arange(m), FC1_N, FC1_K)
+    assert ok, f"worst error / bound = {worst}"
+
+
+def test_fc1_canonical_sampled_rows():
+    """FC1 at the canonical M = 37810: 1024 seeded rows, and the output is
+    the gate|up layout the SwiGLU producer reads (N = 2 x 14336)."""
+    m = 37810
+    a_ref, w_ref, a_dev, w_dev = build_fc1_case(m, seed=12)
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (m, FC1_N)
+    rows = sample_rows(m, 1024, seed=12 + 7)
+    (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, rows, FC1_N, FC1_K)
+    assert ok, f"worst error / bound = {worst}"
