@@ -24,7 +24,7 @@ from . import _lib
 from ._lib import NVFP4Error, load  # noqa: F401
 
 __all__ = ["NVFP4Tensor", "NVFP4Error", "load", "padded_rows", "qdata_bytes", "scale_bytes", "scale_offset",
-           "nvfp4_quantize_weight", "swiglu_nvfp4_quantize", "nvfp4_fc2_gemm", "fc2", "fc2_host",
+           "nvfp4_quantize_weight", "swiglu_nvfp4_quantize", "nvfp4_fc2_gemm", "nvfp4_fc1_swiglu", "fc2", "fc2_host",
            "empty_nvfp4", "read_rec"]
 
 
@@ -144,6 +144,35 @@ def nvfp4_fc2_gemm(a: NVFP4Tensor, w: NVFP4Tensor, out: torch.Tensor | None = No
                                          _ptr(w.rec), m, n, k, _ptr(out), out.stride(0), st_ptr, _stream(stream)),
                    "nvfp4_fc2_gemm")
     return out
+
+
+def nvfp4_fc1_swiglu(a: NVFP4Tensor, w1: NVFP4Tensor, h: torch.Tensor | None = None,
+                     act: NVFP4Tensor | None = None, status: torch.Tensor | None = None,
+                     stream=None) -> tuple[torch.Tensor, NVFP4Tensor]:
+    """FC1 with the SwiGLU producer's first pass in its epilogue, then the
+    quantise pass on h: returns (h [m, f] BF16, the NVFP4 activation of FC2).
+    w1 holds the gate rows then the up rows (2f rows).  The bytes equal
+    swiglu_nvfp4_quantize applied to nvfp4_fc2_gemm(a, w1)."""
+    if a.cols != w1.cols:
+        raise ValueError("activation and weight K differ")
+    if w1.rows % 2:
+        raise ValueError("w1 must hold gate and up rows (an even row count)")
+    m, f, k = a.rows, w1.rows // 2, a.cols
+    if h is None:
+        h = torch.empty(m, f, dtype=torch.bfloat16, device=a.device)
+    if h.dtype != torch.bfloat16 or h.dim() != 2 or h.shape[0] < m or h.shape[1] < f or h.stride(1) != 1:
+        raise ValueError("h must be a bfloat16 [>=m, >=f] tensor with unit column stride")
+    act = act or empty_nvfp4(m, f, a.device)
+    dev = _check_dev(a.qdata, a.scales, a.rec, w1.qdata, w1.scales, w1.rec, h, act.qdata, act.scales, act.rec)
+    st_ptr = ctypes.c_void_p(status.data_ptr()) if status is not None else ctypes.c_void_p(0)
+    with torch.cuda.device(dev):
+        L = load()
+        _lib.check(L.nvfp4_fc1_swiglu(_ptr(a.qdata), _ptr(a.scales), _ptr(a.rec), _ptr(w1.qdata), _ptr(w1.scales),
+                                      _ptr(w1.rec), m, f, k, _ptr(h), h.stride(0), _ptr(act.rec), st_ptr,
+                                      _stream(stream)), "nvfp4_fc1_swiglu")
+        _lib.check(L.nvfp4_quantize_with_amax(_ptr(h), m, f, h.stride(0), _ptr(act.qdata), _ptr(act.scales),
+                                              _ptr(act.rec), _stream(stream)), "nvfp4_quantize_with_amax")
+    return h, act
 
 
 def fc2(gate_up: torch.Tensor, w: NVFP4Tensor, act: NVFP4Tensor | None = None, out: torch.Tensor | None = None,

@@ -29,7 +29,8 @@ EXPORTED = ["nvfp4_padded_rows", "nvfp4_qdata_bytes", "nvfp4_scale_bytes", "nvfp
             "nvfp4_quantize_weight", "swiglu_nvfp4_quantize", "nvfp4_fc2_gemm", "nvfp4_last_error",
             "nvfp4_version", "nvfp4_diag_silu_all", "nvfp4_diag_swiglu", "nvfp4_diag_code_transitions",
             "nvfp4_diag_wait_timeout", "nvfp4_diag_mma_peak", "nvfp4_diag_mma_peak_pairs",
-            "nvfp4_diag_quotient_codes"]
+            "nvfp4_diag_quotient_codes", "nvfp4_fc1_swiglu", "nvfp4_quantize_with_amax",
+            "nvfp4_diag_silu_epilogue"]
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +87,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.nvfp4_diag_mma_peak_pairs.argtypes = []
         L.nvfp4_diag_quotient_codes.restype = st
         L.nvfp4_diag_quotient_codes.argtypes = [u32, u32, vp, vp]
+        L.nvfp4_fc1_swiglu.restype = st
+        L.nvfp4_fc1_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, vp, vp]
+        L.nvfp4_quantize_with_amax.restype = st
+        L.nvfp4_quantize_with_amax.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
+        L.nvfp4_diag_silu_epilogue.restype = st
+        L.nvfp4_diag_silu_epilogue.argtypes = [vp, vp]
         _lib = L
         return _lib
 

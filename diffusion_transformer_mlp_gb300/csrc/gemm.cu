@@ -118,6 +118,54 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
          (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
+// BF16 silu of a gate for the SwiGLU epilogue, the correctly rounded value
+// the producer's table holds ("GB10 component-2 nsys summary": silu in BF16
+// ahead of the multiply by up).  The table (128 KB) cannot sit in shared
+// memory next to the operand ring, so it stays in global memory and the
+// epilogue computes silu(g) = g / (1 + e^-g) in binary32:
+//   e^-g = 2^n 2^f, n = rint(-g log2 e): with log2 e = L_hi + L_lo and L_hi
+//   16 significant bits, -g L_hi is exact for a BF16 g (8 bits), so
+//   f = (-g L_hi - n) + (-g L_lo) carries only the last rounding;
+//   2^f by ex2.approx (|f| <= 1/2), 2^n by the exponent field, the
+//   reciprocal of 1 + e^-g by rcp.approx, one multiply by g.
+// The result is a few units in the last place from silu(g); its BF16
+// rounding is silu's unless it lies within 32 ulp of a BF16 rounding
+// boundary (low half 0x8000), where the table decides, as it does for
+// |g| < 2^-10, g <= -80, -inf and NaN; g >= 8 gives g (the table's closed
+// form).  nvfp4_diag_silu_epilogue runs this for all 65,536 gates against
+// the table.
+__device__ const uint16_t k_silu_tab_epi[65536] = {
+#include "silu_table_full.inc"
+};
+
+constexpr float kLog2eHi = 0x1.7154p+0f;       // log2 e to 16 significant bits
+constexpr float kLog2eLo = 0x1.d94ae0p-18f;    // log2 e - kLog2eHi
+
+__device__ __forceinline__ uint32_t silu_bf16_epi(uint32_t gb) {
+  const float g = __uint_as_float(gb << 16);
+  if (g >= 8.0f) return gb;
+  if (!(g > -80.0f) || fabsf(g) < 0x1p-10f) return k_silu_tab_epi[gb];
+  const float x = __fmul_rn(-g, kLog2eHi);  // exact
+  const float n = rintf(x);
+  const float f = __fmaf_rn(-g, kLog2eLo, __fsub_rn(x, n));
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(f));
+  const float t = __fmul_rn(e, __int_as_float((static_cast<int>(n) + 127) << 23));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, t)));
+  const float s = __fmul_rn(g, r);
+  if (((__float_as_uint(s) + 0x8020u) & 0xFFFFu) <= 64u) return k_silu_tab_epi[gb];
+  return bf16x2_rn(s, 0.0f) & 0xFFFFu;
+}
+
+// h = bf16(silu_bf16(g) * u) for two BF16 (g, u) pairs, as the producer's
+// SwiGLU forms it (mul.rn.bf16x2: the exact product rounded once).
+__device__ __forceinline__ uint32_t swiglu_pair_epi(uint32_t gw, uint32_t uw) {
+  const uint32_t sw = silu_bf16_epi(gw & 0xFFFFu) | (silu_bf16_epi(gw >> 16) << 16);
+  const __nv_bfloat162 h = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&sw),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&uw));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 struct Smem {
   uint8_t* stage;       // STAGES x [A | B]
   uint8_t* sf;          // SF_RING x [A scales | W scales panel 0 | panel 1]
@@ -167,6 +215,12 @@ struct Params {
   int sf_rows;       // 256-byte rows of one 128-row scale panel: k / 32
   uint32_t* dev_status;
   uint64_t wait_limit_cycles;
+  // SwiGLU epilogue (FC1 with the producer's first pass): W rows [0, f) are
+  // the gate and [f, 2f) the up projection; a tile's gate panel comes from
+  // CTA 0 and the matching up panel from CTA 1, so each CTA's accumulator
+  // holds both; h = bf16(silu(g) u) goes to out and max |h| to h_rec.
+  int f;
+  nvfp4_scale_rec* h_rec;
 };
 
 __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag) {
@@ -249,6 +303,7 @@ struct StageWalk {
   }
 };
 
+template <bool kGated>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
@@ -304,7 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // are zero-filled by the TMA and still count their full bytes, so
         // every stage carries 2 x STAGE_BYTES for the leader's barrier.
         const int a_row = mt * PAIR_M + int(rank) * HALF;
-        const int b_row = nt * PAIR_N + int(rank) * HALF;
+        const int b_row = kGated ? (rank == 0 ? nt * HALF : p.f + nt * HALF) : nt * PAIR_N + int(rank) * HALF;
         if (!mbar_wait_bounded(&sm.empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
           report_timeout(p, sm.abort_flag);
           ok = false;
@@ -340,7 +395,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int row0 = w.ks * KSTEPS * 2;  // two 256-byte rows per 512-byte block
         mbar_arrive_expect_tx(&sm.sf_full[r.slot], SF_STAGE_BYTES);
         tma_load_2d(sl, &tmap_sa, &sm.sf_full[r.slot], 0, (mt * 2 + int(rank)) * p.sf_rows + row0, pol_a);
-        tma_load_3d(sl + SFA_BYTES, &tmap_sw, &sm.sf_full[r.slot], 0, row0, nt * 2, pol_w);
+        if constexpr (kGated) {
+          // the gate and the up panel of the tile, one box each
+          tma_load_3d(sl + SFA_BYTES, &tmap_sw, &sm.sf_full[r.slot], 0, row0, nt, pol_w);
+          tma_load_3d(sl + SFA_BYTES + SFW_PANEL_BYTES, &tmap_sw, &sm.sf_full[r.slot], 0, row0, p.f / HALF + nt, pol_w);
+        } else {
+          tma_load_3d(sl + SFA_BYTES, &tmap_sw, &sm.sf_full[r.slot], 0, row0, nt * 2, pol_w);
+        }
       }
     }
   } else if (warp == 1) {
@@ -393,6 +454,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int col0 = ((warp - WARP_EPI0) / 4) * (PAIR_N / 2);  // this warp's half of the columns
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
+    if constexpr (kGated) {
+      // SwiGLU: this warp takes gate columns 64*wh .. +63 and the matching
+      // up columns 128 + 64*wh .. +63 of its 32 rows, 32 of each per load
+      // round; g and u are the BF16 FC1 outputs (accumulator x alpha rounded
+      // as the plain epilogue rounds them) and h goes to columns
+      // nt*128 + 64*wh of the [m, f] output.  The lane keeps max |h| (bit
+      // patterns, as the producer's first pass does) over its stored rows.
+      const int wh = (warp - WARP_EPI0) / 4;
+      uint32_t amax = 0;
+      int local = 0;
+      for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
+        const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
+        if (!warp_wait(sm.tfull, local & 1, p, abort_flag, lane)) {
+          if (lane == 0) report_timeout(p, sm.abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t lane_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL + 64 * wh;
+        const int row = mt * PAIR_M + int(rank) * HALF + q * 32 + lane;
+        const bool row_ok = row < p.m;
+        __nv_bfloat16* hrow = p.out + int64_t(row_ok ? row : 0) * p.ldo + nt * HALF + 64 * wh;
+        // both 32-column rounds are loaded and rounded to BF16 (g and u as
+        // the plain epilogue would store them) before the accumulator goes
+        // back; silu, the product and the stores follow
+        uint32_t gw[2][16], uw[2][16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x32(lane_tmem + 32 * c, r);             // gate
+          tmem_ld_32x32b_x32(lane_tmem + HALF + 32 * c, r + 32);  // up
+          tc_wait_ld();
+          tmem_ld_fence_regs<64>(r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            gw[c][i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+            uw[c][i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[32 + 2 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[32 + 2 * i + 1]), alpha));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = swiglu_pair_epi(gw[c][i], uw[c][i]);
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = max(amax, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+            __nv_bfloat16* dst = hrow + 32 * c;
+            if (p.store32) {
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2)
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * k2), "r"(w[8 * k2]),
+                             "r"(w[8 * k2 + 1]), "r"(w[8 * k2 + 2]), "r"(w[8 * k2 + 3]), "r"(w[8 * k2 + 4]),
+                             "r"(w[8 * k2 + 5]), "r"(w[8 * k2 + 6]), "r"(w[8 * k2 + 7])
+                             : "memory");
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+          }
+        }
+      }
+      // the producer's first pass: one atomic per warp on the record
+      amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+      if (lane == 0 && amax != 0) atomicMax(&p.h_rec->amax_bits, amax);
+    } else {
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
       const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
@@ -452,6 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
       }
+    }
     }
   } else {
     // ------------------------------------------------------------ scale writers (both CTAs)
@@ -554,22 +687,30 @@ nvfp4_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base
 // instead of holding the GPU.
 constexpr uint64_t kDefaultWaitLimitCycles = 4000000000ull;
 
-nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec, const void* w_q,
-                             const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m, int64_t n, int64_t k,
-                             void* out, int64_t ldo, uint32_t* dev_status, cudaStream_t stream,
-                             uint64_t wait_limit_cycles) {
-  if (!a_q || !a_s || !a_rec || !w_q || !w_s || !w_rec || !out)
-    return fail(NVFP4_EINVAL, "nvfp4_fc2_gemm: null pointer");
-  if (m < 1) return fail(NVFP4_EINVAL, "nvfp4_fc2_gemm: m must be >= 1");
-  if (n < HALF || n % HALF != 0) return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: n must be a positive multiple of 128");
-  if (k < 256 || k % 256 != 0) return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: k must be a positive multiple of 256");
-  if (ldo < n) return fail(NVFP4_EINVAL, "nvfp4_fc2_gemm: ldo < n");
+// The plain GEMM (f = 0: out [m, n]) and the SwiGLU-epilogue GEMM (f > 0:
+// W has n = 2f rows, gate then up; out is h [m, f] and h_rec receives max
+// |h|).  `name` prefixes the error messages.
+nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec, const void* w_q,
+                         const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m, int64_t n, int64_t k, void* out,
+                         int64_t ldo, int64_t f, nvfp4_scale_rec* h_rec, uint32_t* dev_status, cudaStream_t stream,
+                         uint64_t wait_limit_cycles, const char* name) {
+  const std::string nm(name);
+  const bool gated = f > 0;
+  if (!a_q || !a_s || !a_rec || !w_q || !w_s || !w_rec || !out || (gated && !h_rec))
+    return fail(NVFP4_EINVAL, nm + ": null pointer");
+  if (m < 1 || f < 0) return fail(NVFP4_EINVAL, nm + ": m must be >= 1");
+  if (gated && (f % HALF != 0 || n != 2 * f))
+    return fail(NVFP4_EUNSUPPORTED, nm + ": f must be a positive multiple of 128 and W must have 2f rows");
+  if (n < HALF || n % HALF != 0) return fail(NVFP4_EUNSUPPORTED, nm + ": n must be a positive multiple of 128");
+  if (k < 256 || k % 256 != 0) return fail(NVFP4_EUNSUPPORTED, nm + ": k must be a positive multiple of 256");
+  const int64_t out_cols = gated ? f : n;
+  if (ldo < out_cols) return fail(NVFP4_EINVAL, nm + ": output leading dimension too small");
   if (ldo % 8 != 0 || !aligned16(a_q) || !aligned16(a_s) || !aligned16(w_q) || !aligned16(w_s) || !aligned16(out) ||
-      !aligned16(a_rec) || !aligned16(w_rec))
-    return fail(NVFP4_EALIGN, "nvfp4_fc2_gemm: pointers must be 16-byte aligned and ldo a multiple of 8");
+      !aligned16(a_rec) || !aligned16(w_rec) || (gated && !aligned16(h_rec)))
+    return fail(NVFP4_EALIGN, nm + ": pointers must be 16-byte aligned and the leading dimension a multiple of 8");
   const int64_t m_pad = nvfp4_padded_rows(m);
   if (m_pad > (int64_t(1) << 30) || n > (int64_t(1) << 24) || k > (int64_t(1) << 24))
-    return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_gemm: problem too large");
+    return fail(NVFP4_EUNSUPPORTED, nm + ": problem too large");
 
   // A and W: 3-D views [k-tile][row][128 B] so one box carries KT k-tiles of
   // 128 rows (each a 128B-swizzled 16 KB tile).  Scales: the A scales as
@@ -606,7 +747,7 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   {
     const cuuint64_t dims[3] = {256, cuuint64_t(k / 32), cuuint64_t(n / 128)};
     const cuuint64_t strides[2] = {256, cuuint64_t(k / 32) * 256};
-    const cuuint32_t box[3] = {256, 2 * KSTEPS, 2};
+    const cuuint32_t box[3] = {256, 2 * KSTEPS, gated ? 1u : 2u};
     if ((st = make_map(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
                        "W scales")) != NVFP4_OK)
       return st;
@@ -621,20 +762,27 @@ nvfp4_status fc2_gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale
   prm.a_rows = static_cast<int>(m_pad);
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
-  prm.num_n_tiles = static_cast<int>((n + PAIR_N - 1) / PAIR_N);
+  prm.num_n_tiles = static_cast<int>(gated ? f / HALF : (n + PAIR_N - 1) / PAIR_N);
   // an odd k-tile count ends with a stage whose second k-tile lies beyond
   // K: the TMA fills it with zeros and no MMA reads it
   prm.num_k_tiles = static_cast<int>(k / 256);
   prm.sf_rows = static_cast<int>(k / 32);
   prm.dev_status = dev_status;
   prm.wait_limit_cycles = wait_limit_cycles;
+  prm.f = static_cast<int>(f);
+  prm.h_rec = h_rec;
+  if (gated) {
+    st = cuda_check(cudaMemsetAsync(h_rec, 0, sizeof(nvfp4_scale_rec), stream), "memset h_rec");
+    if (st != NVFP4_OK) return st;
+  }
 
-  st = cuda_check(cudaFuncSetAttribute(k_fc2_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES),
+  auto kernel = gated ? k_fc2_gemm<true> : k_fc2_gemm<false>;
+  st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES),
                   "cudaFuncSetAttribute(k_fc2_gemm)");
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  k_fc2_gemm<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, prm);
+  kernel<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
@@ -656,6 +804,11 @@ __global__ void k_diag_wait_timeout(uint64_t limit_cycles, uint32_t* dev_status)
     mbar_arrive(&bar);  // complete the phase so the barrier is left idle
   }
 }
+__global__ void k_diag_silu_epilogue(uint16_t* out) {
+  for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < 65536u; g += gridDim.x * blockDim.x)
+    out[g] = static_cast<uint16_t>(silu_bf16_epi(g));
+}
+
 }  // namespace
 
 }  // namespace nvfp4
@@ -666,8 +819,17 @@ extern "C" nvfp4_status nvfp4_fc2_gemm(const void* a_q, const void* a_s, const n
                                        const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m,
                                        int64_t n, int64_t k, void* out_bf16, int64_t ldo, uint32_t* dev_status,
                                        nvfp4_stream_t stream) {
-  return fc2_gemm_launch(a_q, a_s, a_rec, w_q, w_s, w_rec, m, n, k, out_bf16, ldo, dev_status,
-                         reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitCycles);
+  return gemm_launch(a_q, a_s, a_rec, w_q, w_s, w_rec, m, n, k, out_bf16, ldo, 0, nullptr, dev_status,
+                     reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitCycles, "nvfp4_fc2_gemm");
+}
+
+extern "C" nvfp4_status nvfp4_fc1_swiglu(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec,
+                                         const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m,
+                                         int64_t f, int64_t k, void* h_bf16, int64_t ldh, nvfp4_scale_rec* h_rec,
+                                         uint32_t* dev_status, nvfp4_stream_t stream) {
+  if (f < 1) return fail(NVFP4_EINVAL, "nvfp4_fc1_swiglu: f must be >= 1");
+  return gemm_launch(a_q, a_s, a_rec, w_q, w_s, w_rec, m, 2 * f, k, h_bf16, ldh, f, h_rec, dev_status,
+                     reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitCycles, "nvfp4_fc1_swiglu");
 }
 
 extern "C" nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status, nvfp4_stream_t stream) {
@@ -676,4 +838,10 @@ extern "C" nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev
   // cycles at the highest SM clock (2.07 GHz) give at least limit_ns of wall time
   k_diag_wait_timeout<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns * 21 / 10, dev_status);
   return cuda_check(cudaGetLastError(), "launch k_diag_wait_timeout");
+}
+
+extern "C" nvfp4_status nvfp4_diag_silu_epilogue(uint16_t* out, nvfp4_stream_t stream) {
+  if (!out) return fail(NVFP4_EINVAL, "nvfp4_diag_silu_epilogue: null pointer");
+  k_diag_silu_epilogue<<<64, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(out);
+  return cuda_check(cudaGetLastError(), "launch k_diag_silu_epilogue");
 }

@@ -399,8 +399,11 @@ nvfp4_status launch_stream_kernel(K kernel, bool swiglu, int threads, cudaStream
   return cuda_check(cudaGetLastError(), name);
 }
 
+// given_amax: rec->amax_bits already holds max |x| (from the SwiGLU epilogue
+// of FC1), so only pass 2 runs; the plain quantiser is then applied to x.
 nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, bool swiglu, void* qdata,
-                      void* scales, nvfp4_scale_rec* rec, cudaStream_t stream, const char* name) {
+                      void* scales, nvfp4_scale_rec* rec, cudaStream_t stream, const char* name,
+                      bool given_amax = false) {
   if (!x || !qdata || !scales || !rec) return fail(NVFP4_EINVAL, std::string(name) + ": null pointer");
   if (rows < 1 || cols < 16) return fail(NVFP4_EINVAL, std::string(name) + ": rows must be >= 1 and cols >= 16");
   if (cols % 16 != 0) return fail(NVFP4_EUNSUPPORTED, std::string(name) + ": cols must be a multiple of 16");
@@ -415,7 +418,11 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
   uint8_t* q = static_cast<uint8_t*>(qdata);
   uint8_t* s = static_cast<uint8_t*>(scales);
 
-  nvfp4_status st = cuda_check(cudaMemsetAsync(rec, 0, sizeof(nvfp4_scale_rec), stream), "memset rec");
+  nvfp4_status st;
+  if (given_amax)
+    return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows, cols, ld,
+                                rows_pad, q, s, rec);
+  st = cuda_check(cudaMemsetAsync(rec, 0, sizeof(nvfp4_scale_rec), stream), "memset rec");
   if (st != NVFP4_OK) return st;
   if (swiglu) {
     if ((st = launch_stream_kernel(k_amax<true>, true, kThreadsAmaxSwiglu, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
@@ -560,6 +567,13 @@ extern "C" nvfp4_status swiglu_nvfp4_quantize(const void* gate_up_bf16, int64_t 
                                               nvfp4_stream_t stream) {
   return quantize(gate_up_bf16, m, k, ld, true, qdata, scales, rec, reinterpret_cast<cudaStream_t>(stream),
                   "swiglu_nvfp4_quantize");
+}
+
+extern "C" nvfp4_status nvfp4_quantize_with_amax(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                                                 void* qdata, void* scales, nvfp4_scale_rec* rec,
+                                                 nvfp4_stream_t stream) {
+  return quantize(x_bf16, rows, cols, ld, false, qdata, scales, rec, reinterpret_cast<cudaStream_t>(stream),
+                  "nvfp4_quantize_with_amax", true);
 }
 
 extern "C" nvfp4_status nvfp4_diag_silu_all(uint16_t* out, nvfp4_stream_t stream) {

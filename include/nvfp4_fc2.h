@@ -134,6 +134,39 @@ nvfp4_status nvfp4_fc2_gemm(const void* a_q, const void* a_s, const nvfp4_scale_
                             int64_t m, int64_t n, int64_t k, void* out_bf16, int64_t ldo,
                             uint32_t* dev_status, nvfp4_stream_t stream);
 
+/* FC1 with the SwiGLU producer's first pass in its epilogue (the fusion the
+ * pages leave open, "FC2 NVFP4 Scheduling Results", Canonical Operation:
+ * SwiGLU into the NVFP4 quantisation).  The same GEMM as nvfp4_fc2_gemm with
+ * W = [gate; up], 2f rows: each output tile pairs gate rows j and up rows
+ * f + j, and the epilogue writes, for i < m and j < f,
+ *   g = bf16_rn(RN_f32(a_rec.g * w_rec.g) * sum_k A[i,k] W[j,k])
+ *   u = bf16_rn(... W[f + j, k] ...)          (the BF16 FC1 outputs)
+ *   h[i, j] = bf16(bf16(silu(g)) * u)         (silu correctly rounded)
+ * which is byte for byte what nvfp4_fc2_gemm followed by the SwiGLU of
+ * swiglu_nvfp4_quantize computes.  It also writes h_rec->amax_bits = the bit
+ * pattern of max |h| (the producer's first pass), after zeroing h_rec.
+ *   a_q, a_s, a_rec, w_q, w_s, w_rec, m, k   as for nvfp4_fc2_gemm; W has 2f rows
+ *   f >= 128, f % 128 == 0
+ *   h_bf16   device [m, ldh] BF16, ldh >= f, ldh % 8 == 0; other bytes untouched
+ *   h_rec    device record, 16-B aligned: zeroed, then amax_bits set
+ *   dev_status as for nvfp4_fc2_gemm
+ * Follow with nvfp4_quantize_with_amax(h, m, f, ldh, ..., h_rec) for the
+ * NVFP4 activation of FC2: the two calls give the bytes of
+ * swiglu_nvfp4_quantize on FC1's BF16 gate|up output, without writing or
+ * re-reading that 2f-wide output. */
+nvfp4_status nvfp4_fc1_swiglu(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec,
+                              const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec,
+                              int64_t m, int64_t f, int64_t k, void* h_bf16, int64_t ldh,
+                              nvfp4_scale_rec* h_rec, uint32_t* dev_status, nvfp4_stream_t stream);
+
+/* The quantise pass of nvfp4_quantize_weight alone, for a BF16 [rows, cols]
+ * matrix whose global max is already in rec->amax_bits (as
+ * nvfp4_fc1_swiglu leaves it); rec->global_scale and rec->status are
+ * written.  Arguments as for nvfp4_quantize_weight; rec is not zeroed. */
+nvfp4_status nvfp4_quantize_with_amax(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                                      void* qdata, void* scales, nvfp4_scale_rec* rec,
+                                      nvfp4_stream_t stream);
+
 /* Message describing the last non-zero status returned on this host thread. */
 const char* nvfp4_last_error(void);
 

@@ -23,6 +23,12 @@ extern "C" {
  * "GB10 component-2 nsys summary", other_boundaries (separate BF16 silu). */
 nvfp4_status nvfp4_diag_silu_all(uint16_t* out, nvfp4_stream_t stream);
 
+/* out[g] = BF16 bits of the silu the SwiGLU epilogue of nvfp4_fc1_swiglu
+ * computes (binary32 arithmetic, the table near BF16 rounding boundaries)
+ * for every BF16 gate g (65536 entries, device); must equal
+ * nvfp4_diag_silu_all. */
+nvfp4_status nvfp4_diag_silu_epilogue(uint16_t* out, nvfp4_stream_t stream);
+
 /* h[i] = the producer's SwiGLU output for (gate[i], up[i]), BF16 bits,
  * n elements (device arrays). */
 nvfp4_status nvfp4_diag_swiglu(const uint16_t* gate, const uint16_t* up, uint16_t* h, int64_t n,

@@ -98,6 +98,16 @@ def test_gemm_argument_errors():
     assert g(*ok, 4, 128, 320, P16, 128, NUL, NUL) == _lib.NVFP4_EUNSUPPORTED   # k % 256
     assert g(*ok, 4, 128, 256, P16, 64, NUL, NUL) == _lib.NVFP4_EINVAL          # ldo < n
     assert g(*ok, 4, 128, 256, P16, 132, NUL, NUL) == _lib.NVFP4_EALIGN         # ldo % 8
+    f1 = L.nvfp4_fc1_swiglu
+    assert f1(*ok, 4, 0, 256, P16, 128, P16, NUL, NUL) == _lib.NVFP4_EINVAL        # f = 0
+    assert f1(*ok, 4, 192, 256, P16, 192, P16, NUL, NUL) == _lib.NVFP4_EUNSUPPORTED  # f % 128
+    assert f1(*ok, 4, 128, 256, P16, 128, NUL, NUL, NUL) == _lib.NVFP4_EINVAL      # null h_rec
+    assert f1(*ok, 4, 128, 256, P16, 64, P16, NUL, NUL) == _lib.NVFP4_EINVAL       # ldh < f
+    assert f1(*ok, 4, 128, 256, P16, 128, P8, NUL, NUL) == _lib.NVFP4_EALIGN       # h_rec misaligned
+    assert f1(*ok, 4, 128, 320, P16, 128, P16, NUL, NUL) == _lib.NVFP4_EUNSUPPORTED  # k % 256
+    qa = L.nvfp4_quantize_with_amax
+    assert qa(P16, 4, 64, 32, P16, P16, P16, NUL) == _lib.NVFP4_EINVAL             # ld < cols
+    assert qa(P16, 4, 40, 40, P16, P16, P16, NUL) == _lib.NVFP4_EUNSUPPORTED       # cols % 16
     assert g(P8, *ok[1:], 4, 128, 256, P16, 128, NUL, NUL) == _lib.NVFP4_EALIGN  # misaligned A
 
 

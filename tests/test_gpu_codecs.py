@@ -164,3 +164,17 @@ def test_element_codes_match_correctly_rounded_quotient_everywhere():
     sc = _e4m3_values()[None, :] * g[:, None]
     assert seen == int(((sc > 0).sum(axis=1) * 2 * (abits.astype(np.int64) + 1)).sum())
     assert bad == 0
+
+
+def test_epilogue_silu_equals_table_for_every_gate():
+    """The SwiGLU epilogue of nvfp4_fc1_swiglu computes silu in binary32 and
+    asks the table only near BF16 rounding boundaries; for all 65,536 gates it
+    must give the table's (correctly rounded) BF16 silu."""
+    L = _lib.load()
+    tab = torch.empty(65536, dtype=torch.int16, device="cuda")
+    epi = torch.empty(65536, dtype=torch.int16, device="cuda")
+    _lib.check(L.nvfp4_diag_silu_all(_p(tab), _stream()), "silu table")
+    _lib.check(L.nvfp4_diag_silu_epilogue(_p(epi), _stream()), "silu epilogue")
+    torch.cuda.synchronize()
+    diff = (tab != epi).nonzero().flatten().cpu().numpy()
+    assert diff.size == 0, [hex(int(g)) for g in diff[:8]]

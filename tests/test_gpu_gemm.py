@@ -190,3 +190,41 @@ def test_fc1_canonical_sampled_rows():
     rows = sample_rows(m, 1024, seed=12 + 7)
     (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, rows, FC1_N, FC1_K)
     assert ok, f"worst error / bound = {worst}"
+
+
+def _fc1_fused_vs_unfused(m, f, k, seed):
+    """nvfp4_fc1_swiglu + quantise pass against nvfp4_fc2_gemm (BF16 gate|up)
+    + swiglu_nvfp4_quantize: the NVFP4 activation bytes and record are equal,
+    and h equals the producer's SwiGLU of the unfused gate|up."""
+    x = synth.quant_input(m, k, seed=seed)
+    w = synth.weight(2 * f, k, seed=seed)
+    a_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(x))
+    w_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(w))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gate_up = fc2.nvfp4_fc2_gemm(a_dev, w_dev, status=status)
+    act_u = fc2.swiglu_nvfp4_quantize(gate_up)
+    h, act_f = fc2.nvfp4_fc1_swiglu(a_dev, w_dev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert fc2.read_rec(act_f) == fc2.read_rec(act_u)
+    assert torch.equal(act_f.qdata, act_u.qdata)
+    assert torch.equal(act_f.scales, act_u.scales)
+    # h against the producer's own SwiGLU of the unfused output
+    L = fc2._lib.load()
+    g = gate_up[:, :f].contiguous().view(torch.int16)
+    u = gate_up[:, f:].contiguous().view(torch.int16)
+    h_ref = torch.empty_like(g)
+    fc2._lib.check(L.nvfp4_diag_swiglu(fc2._ptr(g), fc2._ptr(u), fc2._ptr(h_ref), g.numel(),
+                                       fc2._stream(None)), "swiglu")
+    torch.cuda.synchronize()
+    assert torch.equal(h.view(torch.int16), h_ref)
+
+
+@pytest.mark.parametrize("m,f,k", [(300, 256, 512), (1, 128, 256), (257, 384, 768)])
+def test_fc1_swiglu_fused_small(m, f, k):
+    _fc1_fused_vs_unfused(m, f, k, seed=m + f + k)
+
+
+def test_fc1_swiglu_fused_canonical():
+    """FC1 at the canonical size, f = 14336, k = 5376, M = 37810."""
+    _fc1_fused_vs_unfused(37810, 14336, 5376, seed=21)
