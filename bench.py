@@ -327,6 +327,20 @@ def fc1_and_chain(dev, x, wq2, act2, out2, fp4_peak, loop, reps: int = 20):
     chain_fused_ms = timed(chain_fused)
     if int(status.item()) != 0 or fc2.read_rec(act2)["status"] != 0:
         raise RuntimeError("device status not OK in the fused chain measurement")
+    # the block's other projections on the same kernel and input width:
+    # qkv (N = 21504) and attention_output (N = 5376), K = 5376
+    proj = {}
+    for name, n_p, dst in (("qkv_gemm", 4 * N, x), ("attention_output_gemm", N, out2)):
+        wp = fc2.nvfp4_quantize_weight(
+            torch.from_numpy(synth.weight(n_p, k1, seed=2).view(np.int16)).view(torch.bfloat16).to(dev))
+        p_ms = timed(lambda: fc2.nvfp4_fc2_gemm(act1, wp, dst, status, stream))
+        p_tf = 2 * M * n_p * k1 / (p_ms * 1e-3) / 1e12
+        proj[name] = {"shape": [M, n_p, k1], "ms": p_ms, "tflops": p_tf, "frac_of_fp4_peak": p_tf / fp4_peak,
+                      "frac_of_fp4_mma_loop_burst": p_tf / loop["burst_tflops"] if loop else None}
+        del wp
+    if int(status.item()) != 0:
+        raise RuntimeError("device status not OK in the projection measurement")
+
     fc1_flop = 2 * M * n1 * k1
     fc1_tflops = fc1_flop / (fc1_ms * 1e-3) / 1e12
     chain_flop = fc1_flop + 2 * M * N * K
@@ -339,6 +353,7 @@ def fc1_and_chain(dev, x, wq2, act2, out2, fp4_peak, loop, reps: int = 20):
             "fc1_swiglu_fused": {"ms": fused_ms, "tflops": fc1_flop / (fused_ms * 1e-3) / 1e12,
                                  "steps": "nvfp4_fc1_swiglu (FC1 + SwiGLU + global max in the epilogue, h BF16 [M, 14336]) "
                                           "+ quantise pass on h"},
+            **proj,
             "mlp_chain_fused": {"ms": chain_fused_ms, "tflops": chain_flop / (chain_fused_ms * 1e-3) / 1e12,
                                 "steps": "fused FC1 -> quantise pass -> FC2 GEMM; weights pre-quantised; "
                                          "bytes identical to mlp_chain's"}}

@@ -228,3 +228,23 @@ def test_fc1_swiglu_fused_small(m, f, k):
 def test_fc1_swiglu_fused_canonical():
     """FC1 at the canonical size, f = 14336, k = 5376, M = 37810."""
     _fc1_fused_vs_unfused(37810, 14336, 5376, seed=21)
+
+
+# The block's other NVFP4 projections on the same kernel.  The pages give
+# their launch grids (296 x 168 and 296 x 42 tiles of 128 x 128): N = 21504
+# for qkv and N = 5376 for attention_output; K is read as the hidden size,
+# 5376 (the pages do not state it; their durations scale with N x 5376).
+@pytest.mark.parametrize("n", [21504, 5376], ids=["qkv", "attention_output"])
+def test_block_projection_sampled_rows(n):
+    m, k = 37810, 5376
+    x = synth.quant_input(m, k, seed=n)
+    w = synth.weight(n, k, seed=n)
+    a_ref = oracle.quantize(x, k, swiglu=False)
+    w_ref = oracle.quantize(w, k, swiglu=False)
+    a_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(x))
+    w_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(w))
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    torch.cuda.synchronize()
+    rows = sample_rows(m, 512, seed=n + 7)
+    (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, rows, n, k)
+    assert ok, f"worst error / bound = {worst}"
