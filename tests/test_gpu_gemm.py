@@ -248,3 +248,26 @@ def test_block_projection_sampled_rows(n):
     rows = sample_rows(m, 512, seed=n + 7)
     (ok, worst), _, _ = gemm_check(out, a_ref, w_ref, rows, n, k)
     assert ok, f"worst error / bound = {worst}"
+
+
+def test_fc1_swiglu_nonfinite_propagates():
+    """An Inf in FC1's input makes FC1's outputs, h and its global max
+    non-finite: the record says so, and FC2 on that activation gives NaN --
+    the same outcome as the unfused path."""
+    m, f, k = 64, 128, 256
+    x = synth.quant_input(m, k, seed=9)
+    w = synth.weight(2 * f, k, seed=9)
+    xd = to_dev_bf16(x)
+    xd[5, 3] = float("inf")
+    a_dev = fc2.nvfp4_quantize_weight(xd)
+    w_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(w))
+    _, act_f = fc2.nvfp4_fc1_swiglu(a_dev, w_dev)
+    act_u = fc2.swiglu_nvfp4_quantize(fc2.nvfp4_fc2_gemm(a_dev, w_dev))
+    torch.cuda.synchronize()
+    assert fc2.read_rec(act_f)["status"] == fc2._lib.NVFP4_ENONFINITE
+    assert fc2.read_rec(act_f) == fc2.read_rec(act_u) or (
+        fc2.read_rec(act_f)["status"] == fc2.read_rec(act_u)["status"])
+    w2 = fc2.nvfp4_quantize_weight(to_dev_bf16(synth.weight(128, f, seed=9)))
+    out = fc2.nvfp4_fc2_gemm(act_f, w2)
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all()
