@@ -254,7 +254,7 @@ def test_fc1_swiglu_nonfinite_propagates():
     """An Inf in FC1's input makes FC1's outputs, h and its global max
     non-finite: the record says so, and FC2 on that activation gives NaN --
     the same outcome as the unfused path."""
-    m, f, k = 64, 128, 256
+    m, f, k = 64, 256, 256
     x = synth.quant_input(m, k, seed=9)
     w = synth.weight(2 * f, k, seed=9)
     xd = to_dev_bf16(x)
