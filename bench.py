@@ -209,8 +209,7 @@ def run_reference(args):
 
 def traffic_record(kernel: str):
     """ncu DRAM bytes per launch for `kernel`, if profiles/traffic.json holds a
-    capture taken on the current source of that kernel."""
-    import hashlib
+    capture taken on the current code of that kernel."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -218,8 +217,21 @@ def traffic_record(kernel: str):
     if not rec:
         return None
     src = os.path.join(ROOT, "diffusion_transformer_mlp_gb300", "csrc", rec["source"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
+    return rec["bytes_per_launch"] if source_hash(src) == rec["source_sha256_16"] else None
+
+
+def source_hash(path: str) -> str:
+    """SHA-256 (16 hex digits) of a kernel's CUDA source and the shared
+    device helpers it includes (common.cuh), with // comments and blank lines
+    removed: the code the counters were taken on."""
+    import hashlib
+    lines = []
+    for line in list(open(path, encoding="utf-8")) + list(open(os.path.join(os.path.dirname(path), "common.cuh"),
+                                                                encoding="utf-8")):
+        code = line.split("//", 1)[0].rstrip() if not line.lstrip().startswith('"') else line.rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
 def fp4_mma_loop(dev, uuid, seconds: float = 1.0, iters: int = 65536):

@@ -49,6 +49,15 @@
 // panels and the whole 43 MB weight through L2.  K is reduced in increasing
 // order inside one CTA: no split-K, no workspace, no atomics, and an output
 // row does not depend on M.
+//
+// k_fc2_gemm<true> is FC1 with the SwiGLU producer's first pass in the
+// epilogue (nvfp4_fc1_swiglu).  W holds the gate rows then the up rows; a
+// pair tile takes 128 gate rows from CTA 0 and the matching 128 up rows
+// from CTA 1, so every CTA's accumulator holds g in columns 0..127 and u in
+// 128..255 for its rows.  The epilogue rounds both to BF16 exactly as the
+// plain epilogue would store them, hands the accumulator back, forms
+// h = bf16(silu_bf16(g) u) and stores it, and keeps max |h| for one atomic
+// per warp on the activation record.
 #include <cuda.h>
 
 #include <cstdio>
