@@ -536,12 +536,12 @@ def run_ours(args):
         kernels.update(extra)
     if gemm_ms >= prod_ms:
         roofline = {"kernel": "k_fc2_gemm", "bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak,
-                    "unit": "TFLOP/s", "frac": gemm_tflops / fp4_peak, "traffic": traffic_record("k_fc2_gemm"),
+                    "unit": "TFLOP/s", "frac": gemm_tflops / fp4_peak, "traffic": traffic_record("k_fc2_gemm") if args.m is None else None,
                     "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"}
     else:
         roofline = {"kernel": "k_quant+k_amax (SwiGLU producer)", "bound": "hbm", "achieved": prod_gbs,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": prod_gbs / peaks["hbm_gbs"],
-                    "traffic": traffic_record("swiglu_producer"),
+                    "traffic": traffic_record("swiglu_producer") if args.m is None else None,
                     "peak_source": f"{peaks['source']} HBM copy"}
 
     if rank == 0:

@@ -44,9 +44,13 @@
 //               the space.  The issuer waits for this drain at every tile
 //               boundary, hence eight warps.
 //
-// Tiles are walked M-panel-major (all N tiles of one 256-row panel, then
-// the next), so the CTAs running at any moment share a few activation
-// panels and the whole 43 MB weight through L2.  K is reduced in increasing
+// Tiles are walked in groups of N tiles: the whole weight when it fits 48 MB
+// (FC2: all 21 N tiles), else 16 MB of it (21 of FC1's 112); each group is walked
+// M-panel-major (all N tiles of the group for one 256-row panel, then the
+// next), so the CTAs running at any moment share a few activation panels
+// and one group's weight rows, which stay in L2 across every panel (one
+// M-panel-major sweep over all 112 FC1 N tiles read its weight ~19 times
+// from DRAM).  K is reduced in increasing
 // order inside one CTA: no split-K, no workspace, no atomics, and an output
 // row does not depend on M.
 //
@@ -220,6 +224,7 @@ struct Params {
   int n;             // weight rows (multiple of 128)
   int num_m_tiles;   // ceil(a_rows / 256)
   int num_n_tiles;   // ceil(n / 256)
+  int group_n;       // N tiles per group of the tile order (see tile_coords)
   int num_k_tiles;   // k / 256
   int sf_rows;       // 256-byte rows of one 128-row scale panel: k / 32
   uint32_t* dev_status;
@@ -231,6 +236,22 @@ struct Params {
   int f;
   nvfp4_scale_rec* h_rec;
 };
+
+// Tile order: the N tiles are cut into groups of group_n; a group is walked
+// M-panel-major (every N tile of the group for one 256-row panel, then the
+// next panel) before the next group starts.  The pairs running at any
+// moment then share a few activation panels and one group's weight rows,
+// which stay in L2 across all panels; with group_n = num_n_tiles this is
+// the plain M-panel-major order.
+__device__ __forceinline__ void tile_coords(int t, const Params& p, int& mt, int& nt) {
+  const int span = p.group_n * p.num_m_tiles;
+  const int g = t / span;
+  const int g0 = g * p.group_n;
+  const int gs = min(p.group_n, p.num_n_tiles - g0);
+  const int r = t - g * span;
+  mt = r / gs;
+  nt = g0 + (r - mt * gs);
+}
 
 __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag) {
   *reinterpret_cast<volatile int*>(abort_flag) = 1;
@@ -362,8 +383,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t pol_a = l2_policy_evict_normal();
       Ring r;
       bool ok = true;
+      int mt = 0, nt = 0, cur_t = -1;
       for (StageWalk w{pair, 0}; w.t < num_tiles && ok; w.next(stages_per_tile, num_pairs), r.next(STAGES)) {
-        const int mt = w.t / p.num_n_tiles, nt = w.t - mt * p.num_n_tiles;
+        if (w.t != cur_t) {  // a new tile: its coordinates, once
+          tile_coords(w.t, p, mt, nt);
+          cur_t = w.t;
+        }
         // Boxes beyond the operands (the last M or N half, a k-tile past K)
         // are zero-filled by the TMA and still count their full bytes, so
         // every stage carries 2 x STAGE_BYTES for the leader's barrier.
@@ -388,8 +413,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t pol_a = l2_policy_evict_normal();
       Ring r;
       bool ok = true;
+      int mt = 0, nt = 0, cur_t = -1;
       for (StageWalk w{pair, 0}; w.t < num_tiles && ok; w.next(stages_per_tile, num_pairs), r.next(SF_RING)) {
-        const int mt = w.t / p.num_n_tiles, nt = w.t - mt * p.num_n_tiles;
+        if (w.t != cur_t) {  // a new tile: its coordinates, once
+          tile_coords(w.t, p, mt, nt);
+          cur_t = w.t;
+        }
         if (!mbar_wait_bounded(&sm.sf_empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
           report_timeout(p, sm.abort_flag);
           ok = false;
@@ -474,7 +503,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t amax = 0;
       int local = 0;
       for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
-        const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
+        int mt, nt;
+        tile_coords(t, p, mt, nt);
         if (!warp_wait(sm.tfull, local & 1, p, abort_flag, lane)) {
           if (lane == 0) report_timeout(p, sm.abort_flag);
           break;
@@ -536,7 +566,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else {
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
-      const int mt = t / p.num_n_tiles, nt = t - mt * p.num_n_tiles;
+      int mt, nt;
+      tile_coords(t, p, mt, nt);
       if (!warp_wait(sm.tfull, local & 1, p, abort_flag, lane)) {
         if (lane == 0) report_timeout(p, sm.abort_flag);
         break;
@@ -772,6 +803,17 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
   prm.num_n_tiles = static_cast<int>(gated ? f / HALF : (n + PAIR_N - 1) / PAIR_N);
+  {
+    // Weight bytes of one N tile (256 rows: E2M1 codes and UE4M3 scales).
+    // A weight that fits 48 MB stays in L2 whole: one group (FC2's 43 MB;
+    // splitting it made every group re-read the activation: 0.92 against
+    // 0.89 ms).  A larger one goes in groups of 16 MB (FC1, qkv: 16 MB
+    // measured best against 8, 24, 32, 48 MB and one group).
+    const int64_t tile_bytes = int64_t(PAIR_N) * (k / 2 + k / 16);
+    const int64_t g = tile_bytes * prm.num_n_tiles <= (int64_t(48) << 20) ? prm.num_n_tiles
+                                                                           : (int64_t(16) << 20) / tile_bytes;
+    prm.group_n = static_cast<int>(g < 1 ? 1 : (g > prm.num_n_tiles ? prm.num_n_tiles : g));
+  }
   // an odd k-tile count ends with a stage whose second k-tile lies beyond
   // K: the TMA fills it with zeros and no MMA reads it
   prm.num_k_tiles = static_cast<int>(k / 256);
