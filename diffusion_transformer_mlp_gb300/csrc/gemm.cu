@@ -258,7 +258,7 @@ __device__ __forceinline__ void report_timeout(const Params& p, int* abort_flag)
   if (p.dev_status != nullptr) atomicExch(p.dev_status, static_cast<uint32_t>(NVFP4_ETIMEOUT));
 }
 
-// One lane of a warp waits; the warp follows its verdict.
+// One lane of a warp waits; the warp follows its result.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
                                           const volatile int* abort_flag, int lane) {
   int ok = 1;

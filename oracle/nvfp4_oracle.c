@@ -22,7 +22,7 @@
  *     global = amax/(6*448), block = RNE-E4M3(block_amax/(6*global)),
  *     element = RNE-E2M1(x/(block*global)).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - silu is rounded once, correctly, to BF16; the SwiGLU product
  *     (exact in binary32) is rounded once to BF16; gate = columns [0,K),
  *     up = columns [K,2K).
