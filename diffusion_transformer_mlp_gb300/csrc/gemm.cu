@@ -60,8 +60,9 @@
 // from CTA 1, so every CTA's accumulator holds g in columns 0..127 and u in
 // 128..255 for its rows.  The epilogue rounds both to BF16 exactly as the
 // plain epilogue would store them, hands the accumulator back, forms
-// h = bf16(silu_bf16(g) u) and stores it, and keeps max |h| for one atomic
-// per warp on the activation record.
+// h = bf16(silu_bf16(g) u) (silu from a 6.5 KB shared-memory slice of the
+// producer's table) and stores it, and keeps max |h| for one atomic per
+// warp on the activation record.
 #include <cuda.h>
 
 #include <cstdio>
@@ -131,49 +132,44 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
          (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
-// BF16 silu of a gate for the SwiGLU epilogue, the correctly rounded value
+// BF16 silu of a gate for the SwiGLU epilogue: the correctly rounded value
 // the producer's table holds ("GB10 component-2 nsys summary": silu in BF16
-// ahead of the multiply by up).  The table (128 KB) cannot sit in shared
-// memory next to the operand ring, so it stays in global memory and the
-// epilogue computes silu(g) = g / (1 + e^-g) in binary32:
-//   e^-g = 2^n 2^f, n = rint(-g log2 e): with log2 e = L_hi + L_lo and L_hi
-//   16 significant bits, -g L_hi is exact for a BF16 g (8 bits), so
-//   f = (-g L_hi - n) + (-g L_lo) carries only the last rounding;
-//   2^f by ex2.approx (|f| <= 1/2), 2^n by the exponent field, the
-//   reciprocal of 1 + e^-g by rcp.approx, one multiply by g.
-// The result is a few units in the last place from silu(g); its BF16
-// rounding is silu's unless it lies within 32 ulp of a BF16 rounding
-// boundary (low half 0x8000), where the table decides, as it does for
-// |g| < 2^-10, g <= -80, -inf and NaN; g >= 8 gives g (the table's closed
-// form).  nvfp4_diag_silu_epilogue runs this for all 65,536 gates against
-// the table.
+// ahead of the multiply by up).  The whole table (128 KB) cannot sit in
+// shared memory next to the operand ring, but the gates FC1 produces are
+// almost all in 2^-10 <= |g| < 8: 13 binades x 128 BF16 mantissas x 2 signs
+// = 3,328 entries (6.5 KB), copied into shared memory at kernel start.  The
+// rest: g >= 8 gives g (the table's closed form, +inf included); |g| < 2^-10,
+// g <= -8, -inf and NaN read the global table.  nvfp4_diag_silu_epilogue
+// runs this for all 65,536 gates against the table.
 __device__ const uint16_t k_silu_tab_epi[65536] = {
 #include "silu_table_full.inc"
 };
 
-constexpr float kLog2eHi = 0x1.7154p+0f;       // log2 e to 16 significant bits
-constexpr float kLog2eLo = 0x1.d94ae0p-18f;    // log2 e - kLog2eHi
+constexpr int kSiluExpLo = 117;                       // biased exponent of 2^-10
+constexpr int kSiluExps = 13;                         // 2^-10 .. 2^3 (exclusive)
+constexpr int kSiluHalf = kSiluExps * 128;            // entries per sign
+constexpr int kSiluSmemBytes = 2 * kSiluHalf * 2;     // 6,656 bytes
 
-__device__ __forceinline__ uint32_t silu_bf16_epi(uint32_t gb) {
-  const float g = __uint_as_float(gb << 16);
-  if (g >= 8.0f) return gb;
-  if (!(g > -80.0f) || fabsf(g) < 0x1p-10f) return k_silu_tab_epi[gb];
-  const float x = __fmul_rn(-g, kLog2eHi);  // exact
-  const float n = rintf(x);
-  const float f = __fmaf_rn(-g, kLog2eLo, __fsub_rn(x, n));
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(f));
-  const float t = __fmul_rn(e, __int_as_float((static_cast<int>(n) + 127) << 23));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, t)));
-  const float s = __fmul_rn(g, r);
-  if (((__float_as_uint(s) + 0x8020u) & 0xFFFFu) <= 64u) return k_silu_tab_epi[gb];
-  return bf16x2_rn(s, 0.0f) & 0xFFFFu;
+__device__ __forceinline__ void fill_silu_smem(uint16_t* tab_s) {
+  for (int i = threadIdx.x; i < 2 * kSiluHalf; i += blockDim.x) {
+    const int sign = i / kSiluHalf, r = i - sign * kSiluHalf;
+    const uint32_t gb = (uint32_t(sign) << 15) | (uint32_t(kSiluExpLo + r / 128) << 7) | uint32_t(r % 128);
+    tab_s[i] = k_silu_tab_epi[gb];
+  }
+}
+
+__device__ __forceinline__ uint32_t silu_bf16_epi(uint32_t gb, const uint16_t* tab_s) {
+  const uint32_t e = (gb >> 7) & 0xFFu;
+  if (e - uint32_t(kSiluExpLo) < uint32_t(kSiluExps))
+    return tab_s[((gb >> 15) ? kSiluHalf : 0) + (e - kSiluExpLo) * 128 + (gb & 0x7Fu)];
+  if (gb < 0x8000u && e >= uint32_t(kSiluExpLo + kSiluExps) && gb <= 0x7F80u) return gb;  // 8 <= g <= +inf
+  return k_silu_tab_epi[gb];
 }
 
 // h = bf16(silu_bf16(g) * u) for two BF16 (g, u) pairs, as the producer's
 // SwiGLU forms it (mul.rn.bf16x2: the exact product rounded once).
-__device__ __forceinline__ uint32_t swiglu_pair_epi(uint32_t gw, uint32_t uw) {
-  const uint32_t sw = silu_bf16_epi(gw & 0xFFFFu) | (silu_bf16_epi(gw >> 16) << 16);
+__device__ __forceinline__ uint32_t swiglu_pair_epi(uint32_t gw, uint32_t uw, const uint16_t* tab_s) {
+  const uint32_t sw = silu_bf16_epi(gw & 0xFFFFu, tab_s) | (silu_bf16_epi(gw >> 16, tab_s) << 16);
   const __nv_bfloat162 h = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&sw),
                                    *reinterpret_cast<const __nv_bfloat162*>(&uw));
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -192,6 +188,7 @@ struct Smem {
   uint64_t* mma_done;
   uint32_t* tmem_slot;
   int* abort_flag;
+  uint16_t* silu;       // the SwiGLU epilogue's silu entries (k_fc2_gemm<true> only)
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
@@ -209,9 +206,11 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.mma_done = s.tempty + 1;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
+  s.silu = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + BAR_BYTES);
   return s;
 }
 static_assert((2 * STAGES + 2 * SF_RING + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
+static_assert(SMEM_BYTES + kSiluSmemBytes <= 232448, "shared memory budget of the SwiGLU epilogue");
 
 struct Params {
   const nvfp4_scale_rec* a_rec;
@@ -369,6 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefetch_tmap(&tmap_sa);
     prefetch_tmap(&tmap_sw);
   }
+  if constexpr (kGated) fill_silu_smem(sm.silu);
   if (warp == 1) tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -540,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 2; ++c) {
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = swiglu_pair_epi(gw[c][i], uw[c][i]);
+          for (int i = 0; i < 16; ++i) w[i] = swiglu_pair_epi(gw[c][i], uw[c][i], sm.silu);
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) amax = max(amax, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
@@ -828,12 +828,13 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   }
 
   auto kernel = gated ? k_fc2_gemm<true> : k_fc2_gemm<false>;
-  st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES),
+  const int smem = gated ? SMEM_BYTES + kSiluSmemBytes : SMEM_BYTES;
+  st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                   "cudaFuncSetAttribute(k_fc2_gemm)");
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  kernel<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(ta, tw, tsa, tsw, prm);
+  kernel<<<2 * pairs, THREADS, smem, stream>>>(ta, tw, tsa, tsw, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
@@ -856,8 +857,11 @@ __global__ void k_diag_wait_timeout(uint64_t limit_cycles, uint32_t* dev_status)
   }
 }
 __global__ void k_diag_silu_epilogue(uint16_t* out) {
+  __shared__ uint16_t tab_s[2 * kSiluHalf];
+  fill_silu_smem(tab_s);
+  __syncthreads();
   for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < 65536u; g += gridDim.x * blockDim.x)
-    out[g] = static_cast<uint16_t>(silu_bf16_epi(g));
+    out[g] = static_cast<uint16_t>(silu_bf16_epi(g, tab_s));
 }
 
 }  // namespace
