@@ -550,6 +550,34 @@ __global__ void k_diag_quotient_codes(uint32_t a_first, uint32_t a_count, unsign
   atomicAdd(&counts[1], seen);
 }
 
+// Every (global max, block max) through block_scale_code, against the
+// definition E4M3(RN(bmax / d)) with d = RN(6 g), g = RN(A / 2688) as pass 2
+// forms them and RN(bmax / d) the correctly rounded division.  Global
+// maxima A are the BF16 patterns a_first .. a_first + a_count - 1; block
+// maxima every finite non-negative BF16 pattern (above A too, so that the
+// saturating end of the encoder is reached).
+// counts[0] += codes that differ, counts[1] += codes compared.
+__global__ void k_diag_block_scale_codes(uint32_t a_first, uint32_t a_count, unsigned long long* counts) {
+  constexpr uint32_t kFinite = 0x7F80u;  // non-negative finite BF16 patterns
+  unsigned long long bad = 0, seen = 0;
+  const uint64_t items = uint64_t(a_count) * kFinite;
+  for (uint64_t it = blockIdx.x * uint64_t(blockDim.x) + threadIdx.x; it < items;
+       it += uint64_t(gridDim.x) * blockDim.x) {
+    const uint32_t bbits = uint32_t(it % kFinite);
+    const uint32_t abits = a_first + uint32_t(it / kFinite);
+    const float g = __fdiv_rn(bf16_to_f32(abits), 2688.0f);
+    const float d = __fmul_rn(6.0f, g);
+    const float rd = d == 0.0f ? 0.0f : __frcp_rn(d);
+    const float bmax = bf16_to_f32(bbits);
+    const uint32_t got = block_scale_code(bmax, d, rd);
+    const uint32_t want = d == 0.0f ? 0u : e4m3_code(__fdiv_rn(bmax, d));
+    bad += got != want ? 1u : 0u;
+    ++seen;
+  }
+  atomicAdd(&counts[0], bad);
+  atomicAdd(&counts[1], seen);
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -611,4 +639,13 @@ extern "C" nvfp4_status nvfp4_diag_quotient_codes(uint32_t a_first, uint32_t a_c
   k_diag_quotient_codes<<<sm_count() * 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       a_first, a_count, reinterpret_cast<unsigned long long*>(counts));
   return cuda_check(cudaGetLastError(), "launch k_diag_quotient_codes");
+}
+
+extern "C" nvfp4_status nvfp4_diag_block_scale_codes(uint32_t a_first, uint32_t a_count, uint64_t* counts,
+                                                     nvfp4_stream_t stream) {
+  if (!counts || a_count < 1 || a_first >= 0x7F80u || a_count > 0x7F80u - a_first)
+    return fail(NVFP4_EINVAL, "nvfp4_diag_block_scale_codes: bad arguments");
+  k_diag_block_scale_codes<<<sm_count() * 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      a_first, a_count, reinterpret_cast<unsigned long long*>(counts));
+  return cuda_check(cudaGetLastError(), "launch k_diag_block_scale_codes");
 }

@@ -68,6 +68,33 @@ nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status,
 nvfp4_status nvfp4_diag_quotient_codes(uint32_t a_first, uint32_t a_count, uint64_t* counts,
                                        nvfp4_stream_t stream);
 
+/* The block-scale encoder of pass 2 swept against its definition ("GB10
+ * component-2 nsys summary", nvfp4: scale finalize, then block scales from
+ * block absmax; the two-level NVFP4 recipe bs = E4M3(block_amax / (6 g))):
+ * for every global max A among the BF16 patterns a_first .. a_first +
+ * a_count - 1 (g = RN(A / 2688), d = RN(6 g)) and every finite non-negative
+ * BF16 block max b, the producer's code is compared with E4M3(RN(b / d)),
+ * RN(b / d) the correctly rounded division (0 when d == 0).  counts
+ * (device, two uint64, zeroed by the caller) receives += {codes that
+ * differ, codes compared}.  a_first + a_count <= 0x7F80, a_count >= 1, else
+ * NVFP4_EINVAL.  All 32,640 maxima (about 10^9 pairs) take well under a
+ * second. */
+nvfp4_status nvfp4_diag_block_scale_codes(uint32_t a_first, uint32_t a_count, uint64_t* counts,
+                                          nvfp4_stream_t stream);
+
+/* The tensor core's reading of packed E2M1 bytes ("FC2 NVFP4 Scheduling
+ * Results", Canonical Operation: packed E2M1 operands).  qdata holds 128
+ * rows of 16 bytes (32 E2M1 elements each, row-major, device, 16-B
+ * aligned); one tcgen05.mma.kind::f8f6f4 multiplies them by the 32 x 32
+ * identity in E4M3 (one byte per element), so out[r * 32 + n] (device
+ * float, 128 x 32) is the value the tensor core gives element n of row r.
+ * An E2M1 x E2M1 GEMM cannot show which nibble holds which element (the
+ * same swap in both operands leaves every dot product unchanged); this
+ * can.  NVFP4_ETIMEOUT goes to *dev_status (device uint32, may be NULL) if
+ * the MMA's completion is not seen within about a second. */
+nvfp4_status nvfp4_diag_tc_e2m1_read(const uint8_t* qdata, float* out, uint32_t* dev_status,
+                                     nvfp4_stream_t stream);
+
 /* Dense NVFP4 tensor-core throughput of this GPU, the denominator of the
  * GEMM's roofline ("FC2 NVFP4 Scheduling Results", Canonical Operation: the
  * FC2 is a dense E2M1 x E2M1 contraction with UE4M3 vector-16 scales).

@@ -9,9 +9,11 @@ What it computes follows "FC2 NVFP4 Scheduling Results" (Canonical Operation)
 and "GB10 component-2 nsys summary" (nvfp4, native_pack_validation,
 other_boundaries); each C function cites its passage in ``nvfp4_oracle.c``.
 
-Pinned by tests/test_oracle_*.py.  Nibble order inside a QDATA byte is
-parity unpinned beyond self-consistency (a swap in both operands cancels in
-the GEMM, and no page prints packed bytes).
+Pinned on the CPU by tests/test_oracle_pins.py.  The byte conventions no
+page prints are pinned on the GPU against readers outside this repository
+(tests/test_gpu_pins.py): the nibble order by the tensor core's own reading
+of the oracle's QDATA, the tiled scale layout by cuBLASLt's block-scaled
+NVFP4 matmul on the oracle's bytes.
 """
 from __future__ import annotations
 
@@ -78,6 +80,8 @@ def lib():
             L.oracle_silu_table.argtypes = [u16p]
             L.oracle_swiglu_bf16.restype = ctypes.c_uint16
             L.oracle_swiglu_bf16.argtypes = [ctypes.c_uint16, ctypes.c_uint16, u16p]
+            L.oracle_swiglu_rows.restype = ctypes.c_int
+            L.oracle_swiglu_rows.argtypes = [u16p, i64, i64, i64, u16p]
             L.oracle_padded_rows.restype = i64
             L.oracle_padded_rows.argtypes = [i64]
             L.oracle_scale_cols_padded.restype = i64
@@ -92,6 +96,8 @@ def lib():
             L.oracle_gemm_rows.restype = ctypes.c_int
             L.oracle_gemm_rows.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float,
                                            i64, i64, i64p, i64, f64p]
+            L.oracle_epilogue_bf16.restype = None
+            L.oracle_epilogue_bf16.argtypes = [f64p, i64, ctypes.c_float, u16p]
             _lib = L
     return _lib
 
@@ -136,6 +142,19 @@ def silu_table() -> tuple[np.ndarray, int]:
 
 def swiglu_bf16(g: int, u: int) -> int:
     return int(lib().oracle_swiglu_bf16(g, u, None))
+
+
+def swiglu_rows(x: np.ndarray, cols: int) -> np.ndarray:
+    """SwiGLU of a gate|up BF16 matrix (uint16 bits [rows, ld >= 2 cols]):
+    h [rows, cols] as BF16 bits, the tensor the activation producer
+    quantises."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    rows, ld = x.shape
+    h = np.empty((rows, cols), dtype=np.uint16)
+    st = lib().oracle_swiglu_rows(_p(x, ctypes.c_uint16), rows, cols, ld, _p(h, ctypes.c_uint16))
+    if st != OK:
+        raise ValueError(f"oracle_swiglu_rows rejected its arguments (status {st})")
+    return h
 
 
 # ---- sizes and layout ------------------------------------------------------
@@ -204,6 +223,15 @@ def gemm_rows(a_q, a_s, ga, w_q, w_s, gw, n: int, k: int, rows: np.ndarray) -> n
                                 n, k, _p(rows, ctypes.c_int64), rows.size, _p(out, ctypes.c_double))
     if st != OK:
         raise ValueError(f"oracle_gemm_rows rejected its arguments (status {st})")
+    return out
+
+
+def epilogue_bf16(ref: np.ndarray, alpha: float) -> np.ndarray:
+    """BF16 bits RNE(RN_f32(float32(ref) * alpha)): the GPU output for inputs
+    whose FP32 accumulation is exact (every partial sum a binary32 value)."""
+    ref = np.ascontiguousarray(ref, dtype=np.float64)
+    out = np.empty(ref.shape, dtype=np.uint16)
+    lib().oracle_epilogue_bf16(_p(ref, ctypes.c_double), ref.size, float(np.float32(alpha)), _p(out, ctypes.c_uint16))
     return out
 
 

@@ -32,10 +32,13 @@
  *   - rows padded to a multiple of 128, pad rows and pad scale columns zero.
  *   - a non-finite amax gives status 4, global scale NaN, all-zero output.
  *
- * Parity pins live in tests/test_oracle_*.py (brute-force code tables,
+ * Parity pins live in tests/test_oracle_pins.py (brute-force code tables,
  * hand-worked blocks, round-trip bounds, closed-form byte counts, an
- * independent FP64 matmul on tiny shapes).  Nibble order is unpinned beyond
- * self-consistency: a consistent swap in both GEMM operands cancels.
+ * independent FP64 matmul on tiny shapes) and tests/test_gpu_pins.py: the
+ * nibble order, which a GEMM of two packed operands cannot show (the same
+ * swap in both cancels), against the tensor core's own reading of these
+ * bytes; the tiled scale layout against a library's block-scaled NVFP4
+ * matmul on these bytes.
  *
  * Arithmetic: every float operation below is one IEEE binary32 (or binary64
  * where stated) operation; build with -ffp-contract=off so that no two are
@@ -219,6 +222,24 @@ uint16_t oracle_swiglu_bf16(uint16_t g, uint16_t u, const uint16_t* silu_tab) {
   return oracle_f32_to_bf16(p);
 }
 
+/* h [rows, cols] (row stride cols) = the SwiGLU of every element of a
+ * gate|up matrix x [rows, ld] (gate in columns [0, cols), up in [cols,
+ * 2 cols)): h = RNE_bf16(silu_bf16(g) * u) as above, the tensor the
+ * producer quantises ("GB10 component-2 nsys summary", other_boundaries: a
+ * BF16 silu, then a BF16 multiply). */
+int oracle_swiglu_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint16_t* h) {
+  if (!x || !h || rows < 0 || cols < 1 || ld < 2 * cols) return ORACLE_EINVAL;
+  uint16_t* silu_tab = (uint16_t*)malloc(65536 * sizeof(uint16_t));
+  if (!silu_tab) return ORACLE_EINVAL;
+  oracle_silu_table(silu_tab);
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t j = 0; j < cols; ++j)
+      h[r * cols + j] = oracle_swiglu_bf16(x[r * ld + j], x[r * ld + cols + j], silu_tab);
+  free(silu_tab);
+  return ORACLE_OK;
+}
+
 /* ---------------- Sizes and the scale layout ------------------------------- */
 
 int64_t oracle_padded_rows(int64_t rows) { return (rows + 127) / 128 * 128; }
@@ -366,4 +387,19 @@ int oracle_gemm_rows(const uint8_t* a_q, const uint8_t* a_s, float ga,
   }
   free(wd); free(ad); free(wrows);
   return ORACLE_OK;
+}
+
+/* The GEMM epilogue's rounding of accumulator values ("FC2 NVFP4 Scheduling
+ * Results", Canonical Operation: FP32 accumulation and scalars, BF16
+ * output): out[i] = RNE_bf16(RN_f32(acc_i * alpha)) with acc_i the binary32
+ * accumulator, taken here as (float)ref[i].  That equals the tensor core's
+ * accumulator whenever every partial sum of the dot product is exact in
+ * binary32 (e.g. E2M1 values with unit block scales: multiples of 1/4 far
+ * below 2^22), so for such inputs the whole GEMM output is known exactly. */
+void oracle_epilogue_bf16(const double* ref, int64_t n, float alpha, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    float acc = (float)ref[i];
+    out[i] = oracle_f32_to_bf16(acc * alpha);
+  }
 }

@@ -11,7 +11,8 @@ import torch
 import diffusion_transformer_mlp_gb300 as fc2
 import oracle
 import synth
-from _util import gemm_check, sample_rows, to_dev_bf16
+from _edge import grid_matrix
+from _util import compare_quant, gemm_check, sample_rows, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -95,7 +96,6 @@ def test_gemm_ragged_m(m):
     1024 sampled rows (always including the last row), 50 back-to-back runs
     with identical bytes."""
     n, k = 5376, 14336
-    from _util import compare_quant
     a_ref, w_ref, a_dev, w_dev, xd = build_case(m, n, k, seed=0)
     assert compare_quant(a_dev, *a_ref, m, k) is None
     out0 = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
@@ -193,9 +193,10 @@ def test_fc1_canonical_sampled_rows():
 
 
 def _fc1_fused_vs_unfused(m, f, k, seed):
-    """nvfp4_fc1_swiglu + quantise pass against nvfp4_fc2_gemm (BF16 gate|up)
-    + swiglu_nvfp4_quantize: the NVFP4 activation bytes and record are equal,
-    and h equals the producer's SwiGLU of the unfused gate|up."""
+    """Composition check on the activation law: nvfp4_fc1_swiglu + quantise
+    pass against nvfp4_fc2_gemm (BF16 gate|up) + swiglu_nvfp4_quantize give
+    the same NVFP4 activation bytes and record, and h equals the producer's
+    SwiGLU of the unfused gate|up."""
     x = synth.quant_input(m, k, seed=seed)
     w = synth.weight(2 * f, k, seed=seed)
     a_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(x))
@@ -228,6 +229,81 @@ def test_fc1_swiglu_fused_small(m, f, k):
 def test_fc1_swiglu_fused_canonical():
     """FC1 at the canonical size, f = 14336, k = 5376, M = 37810."""
     _fc1_fused_vs_unfused(37810, 14336, 5376, seed=21)
+
+
+def exact_case(m, n, k, seed):
+    """NVFP4 operands whose FP32 accumulation is exact (grid inputs, unit
+    scales; tests/_edge.py), with the oracle's bytes for both, the device
+    tensors, and the oracle's exact FP64 products for all rows."""
+    x = grid_matrix(m, k, seed, 0)
+    w = grid_matrix(n, k, seed + 1, 16)
+    a_ref = oracle.quantize(x, k, swiglu=False)
+    w_ref = oracle.quantize(w, k, swiglu=False)
+    a_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(x))
+    w_dev = fc2.nvfp4_quantize_weight(to_dev_bf16(w))
+    torch.cuda.synchronize()
+    assert compare_quant(a_dev, *a_ref, m, k) is None and compare_quant(w_dev, *w_ref, n, k) is None
+    return a_ref, w_ref, a_dev, w_dev
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 256, 1024), (1000, 384, 2048), (130, 5376, 14336), (129, 28672, 5376)])
+def test_gemm_bit_exact_when_accumulation_is_exact(m, n, k):
+    """Every output element equals the oracle's RNE_bf16(RN(acc * alpha)) bit
+    for bit when no partial sum rounds: the epilogue's arithmetic (alpha,
+    the binary32 product, the BF16 rounding) pinned exactly, not within a
+    tolerance."""
+    a_ref, w_ref, a_dev, w_dev = exact_case(m, n, k, seed=m + n + k)
+    out = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    ref = oracle.gemm_rows(a_ref[0], a_ref[1], a_ref[2]["global_scale"], w_ref[0], w_ref[1],
+                           w_ref[2]["global_scale"], n, k, np.arange(m))
+    alpha = np.float32(a_ref[2]["global_scale"]) * np.float32(w_ref[2]["global_scale"])
+    want = oracle.epilogue_bf16(ref, alpha)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} elements differ; first {tuple(bad[0])}"
+
+
+def _fc1_fused_vs_oracle(m, f, k, seed, rows=None):
+    """nvfp4_fc1_swiglu + its quantise pass against the oracle on operands
+    whose FC1 accumulation is exact: the oracle forms FC1's BF16 gate|up
+    (its epilogue rounding of the exact FP64 products), then h and the
+    two-pass NVFP4 bytes of h.  h is compared bit for bit on `rows` (all
+    rows by default); with all rows the QDATA, scales and record are too.
+    With a row sample, the record's max is checked against the h the same
+    call wrote."""
+    a_ref, w_ref, a_dev, w_dev = exact_case(m, 2 * f, k, seed)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h, act = fc2.nvfp4_fc1_swiglu(a_dev, w_dev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.arange(m) if rows is None else rows
+    ref = oracle.gemm_rows(a_ref[0], a_ref[1], a_ref[2]["global_scale"], w_ref[0], w_ref[1],
+                           w_ref[2]["global_scale"], 2 * f, k, sel)
+    alpha = np.float32(a_ref[2]["global_scale"]) * np.float32(w_ref[2]["global_scale"])
+    gate_up = oracle.epilogue_bf16(ref, alpha)
+    h_want = oracle.swiglu_rows(gate_up, f)
+    h_got = h[torch.from_numpy(sel).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    bad = np.argwhere(h_got != h_want)
+    assert bad.size == 0, f"h: {len(bad)} elements differ; first {tuple(bad[0])}"
+    if rows is None:
+        q, s, rec = oracle.quantize(gate_up, f, swiglu=True)
+        err = compare_quant(act, q, s, rec, m, f)
+        assert err is None, err
+    else:
+        hmax = h.float().abs().max().item()
+        assert fc2.read_rec(act)["amax_bits"] == int(np.float32(hmax).view(np.uint32))
+
+
+@pytest.mark.parametrize("m,f,k", [(300, 256, 512), (1, 128, 256), (257, 384, 768), (513, 1024, 5376)])
+def test_fc1_swiglu_fused_matches_oracle(m, f, k):
+    _fc1_fused_vs_oracle(m, f, k, seed=m + f + k)
+
+
+def test_fc1_swiglu_fused_matches_oracle_canonical_rows():
+    """Canonical FC1 shape (M = 37810, f = 14336, k = 5376): h on 256 seeded
+    rows (always the first and the last) bit-exact against the oracle."""
+    m = 37810
+    _fc1_fused_vs_oracle(m, 14336, 5376, seed=31, rows=sample_rows(m, 256, seed=31 + 7))
 
 
 # The block's other NVFP4 projections on the same kernel.  The pages give

@@ -1,6 +1,7 @@
 """Producer parity on the GPU: QDATA, scale bytes and the global-scale record
 of both quantisers are bit-exact against the oracle, for small shapes that
-span several tiles and a ragged tail, the hand-worked blocks, the
+span several tiles and a ragged tail, the hand-worked blocks, inputs built
+to reach every UE4M3 block-scale code and the recipe's ties and zeros, the
 quantise-only workload at feature widths 5376 / 7168 / 14336 (M = 37,810,
 padded), and the canonical SwiGLU producer (M = 37,810, K = 14,336)."""
 import json
@@ -13,6 +14,7 @@ import torch
 import diffusion_transformer_mlp_gb300 as fc2
 import oracle
 import synth
+from _edge import E4M3, edge_matrix, swiglu_input
 from _util import compare_quant, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
@@ -70,6 +72,40 @@ def test_hand_worked_blocks_on_device():
     rec = fc2.read_rec(dev)
     assert rec["global_scale"] == row["global_scale"] and rec["status"] == 0
     assert not dev.qdata[1:].any() and int(dev.scales.sum()) == sum(row["scale_codes"])
+
+
+@pytest.mark.parametrize("rows,cols", [(300, 16), (300, 48), (300, 272), (257, 1024)])
+def test_edge_blocks_bit_exact(rows, cols):
+    """Every UE4M3 scale code 0x00..0x7E (subnormals included), ratios half
+    way between two codes, ratios that round to 0, all-zero and all -0
+    blocks inside a non-zero tensor, negatives that encode as E2M1 -0, and
+    element values on E2M1 rounding midpoints; both quantisers (the SwiGLU
+    one through gate = 8, up = h / 8, whose SwiGLU is h)."""
+    x = edge_matrix(rows, cols, seed=rows + cols)
+    q, s, rec = oracle.quantize(x, cols, swiglu=False)
+    assert rec["global_scale"] == np.float32(1.0)
+    codes = {int(s[oracle.scale_offset(r, b, cols)]) for r in range(rows) for b in range(cols // 16)}
+    assert codes == set(range(len(E4M3)))
+    err = compare_quant(run_weight(x, cols), q, s, rec, rows, cols)
+    assert err is None, err
+    gu = swiglu_input(x)
+    qs, ss, recs = oracle.quantize(gu, cols, swiglu=True)
+    assert np.array_equal(qs, q) and np.array_equal(ss, s)
+    err = compare_quant(run_swiglu(gu, cols), qs, ss, recs, rows, cols)
+    assert err is None, err
+
+
+@pytest.mark.parametrize("factor", [0.3701171875, 1.0009765625e-30, 3.0e30])
+def test_edge_blocks_other_global_scales(factor):
+    """The same blocks scaled by a BF16 factor (truncated toward zero), so the
+    global scale is no longer 1 and reaches the tiny and huge ends of
+    binary32."""
+    rows, cols = 300, 272
+    xf = (edge_matrix(rows, cols, seed=7).astype(np.uint32) << 16).view(np.float32) * np.float32(factor)
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)
+    q, s, rec = oracle.quantize(x, cols, swiglu=False)
+    err = compare_quant(run_weight(x, cols), q, s, rec, rows, cols)
+    assert err is None, err
 
 
 def test_zero_input_and_nonfinite_status():

@@ -397,3 +397,31 @@ def test_gemm_tolerance_helper():
     assert ok
     ok, _ = oracle.check_gemm_tolerance(ref * 1.05, ref)
     assert not ok
+
+
+def test_swiglu_rows_matches_scalar_swiglu():
+    """The array SwiGLU equals the scalar one element by element (both read
+    gate from the first half of a row and up from the second)."""
+    x = synth.activation(7, 48, seed=5)
+    h = oracle.swiglu_rows(x, 48)
+    want = np.array([[oracle.swiglu_bf16(int(x[r, j]), int(x[r, 48 + j])) for j in range(48)] for r in range(7)])
+    assert np.array_equal(h, want)
+    # a gate of 8 leaves up times 8 (silu rounds to 8 in BF16), which the
+    # edge-case GPU tests use to reach a chosen h through the SwiGLU producer
+    gu = np.zeros((1, 2), dtype=np.uint16)
+    gu[0, 0] = 0x4100  # 8.0
+    gu[0, 1] = 0x3FC0  # 1.5
+    assert oracle.swiglu_rows(gu, 1)[0, 0] == 0x4140  # 12.0
+
+
+def test_edge_inputs_reach_every_scale_code():
+    """The edge-case inputs of the GPU parity tests do reach every UE4M3
+    block-scale code, at every width they are used with."""
+    from _edge import E4M3, edge_matrix
+    assert np.array_equal(E4M3, [oracle.e4m3_value(c) for c in range(127)])
+    for rows, cols in [(300, 16), (300, 48), (300, 272)]:
+        x = edge_matrix(rows, cols, seed=rows + cols)
+        _, s, rec = oracle.quantize(x, cols, swiglu=False)
+        assert rec["global_scale"] == np.float32(1.0)
+        codes = {int(s[oracle.scale_offset(r, b, cols)]) for r in range(rows) for b in range(cols // 16)}
+        assert codes == set(range(127))
