@@ -94,6 +94,22 @@ def _check_dev(*ts: torch.Tensor) -> torch.device:
     return dev
 
 
+def _check_nvfp4(t: NVFP4Tensor, rows: int, cols: int, name: str) -> NVFP4Tensor:
+    """The buffers of `t` can hold an NVFP4 [rows, cols] tensor: the shape it
+    records is (rows, cols), and QDATA, scales and record are contiguous
+    uint8 buffers of at least the bytes the kernels read or write."""
+    if t.rows != rows or t.cols != cols:
+        raise ValueError(f"{name} holds a [{t.rows}, {t.cols}] NVFP4 tensor, [{rows}, {cols}] is needed")
+    need = {"qdata": qdata_bytes(rows, cols), "scales": scale_bytes(rows, cols), "rec": 16}
+    for field, n in need.items():
+        b = getattr(t, field)
+        if b.dtype != torch.uint8 or not b.is_contiguous():
+            raise ValueError(f"{name}.{field} must be a contiguous uint8 tensor")
+        if b.numel() < n:
+            raise ValueError(f"{name}.{field} has {b.numel()} bytes, {n} are needed")
+    return t
+
+
 def _bf16_matrix(x: torch.Tensor, name: str) -> torch.Tensor:
     if x.dtype != torch.bfloat16 or x.dim() != 2:
         raise ValueError(f"{name} must be a 2-D bfloat16 tensor")
@@ -105,7 +121,7 @@ def _bf16_matrix(x: torch.Tensor, name: str) -> torch.Tensor:
 def nvfp4_quantize_weight(w: torch.Tensor, out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
     _bf16_matrix(w, "w")
     rows, cols = w.shape
-    out = out or empty_nvfp4(rows, cols, w.device)
+    out = _check_nvfp4(out, rows, cols, "out") if out is not None else empty_nvfp4(rows, cols, w.device)
     dev = _check_dev(w, out.qdata, out.scales, out.rec)
     with torch.cuda.device(dev):
         _lib.check(load().nvfp4_quantize_weight(_ptr(w), rows, cols, w.stride(0), _ptr(out.qdata), _ptr(out.scales),
@@ -119,7 +135,7 @@ def swiglu_nvfp4_quantize(gate_up: torch.Tensor, out: NVFP4Tensor | None = None,
     if two_k % 2:
         raise ValueError("gate_up must have an even number of columns (gate | up)")
     k = two_k // 2
-    out = out or empty_nvfp4(m, k, gate_up.device)
+    out = _check_nvfp4(out, m, k, "out") if out is not None else empty_nvfp4(m, k, gate_up.device)
     dev = _check_dev(gate_up, out.qdata, out.scales, out.rec)
     with torch.cuda.device(dev):
         _lib.check(load().swiglu_nvfp4_quantize(_ptr(gate_up), m, k, gate_up.stride(0), _ptr(out.qdata),
@@ -133,6 +149,8 @@ def nvfp4_fc2_gemm(a: NVFP4Tensor, w: NVFP4Tensor, out: torch.Tensor | None = No
     if a.cols != w.cols:
         raise ValueError("activation and weight K differ")
     m, n, k = a.rows, w.rows, a.cols
+    _check_nvfp4(a, m, k, "a")
+    _check_nvfp4(w, n, k, "w")
     if out is None:
         out = torch.empty(m, n, dtype=torch.bfloat16, device=a.device)
     if out.dtype != torch.bfloat16 or out.dim() != 2 or out.shape[0] < m or out.shape[1] < n or out.stride(1) != 1:
@@ -158,11 +176,13 @@ def nvfp4_fc1_swiglu(a: NVFP4Tensor, w1: NVFP4Tensor, h: torch.Tensor | None = N
     if w1.rows % 2:
         raise ValueError("w1 must hold gate and up rows (an even row count)")
     m, f, k = a.rows, w1.rows // 2, a.cols
+    _check_nvfp4(a, m, k, "a")
+    _check_nvfp4(w1, 2 * f, k, "w1")
     if h is None:
         h = torch.empty(m, f, dtype=torch.bfloat16, device=a.device)
     if h.dtype != torch.bfloat16 or h.dim() != 2 or h.shape[0] < m or h.shape[1] < f or h.stride(1) != 1:
         raise ValueError("h must be a bfloat16 [>=m, >=f] tensor with unit column stride")
-    act = act or empty_nvfp4(m, f, a.device)
+    act = _check_nvfp4(act, m, f, "act") if act is not None else empty_nvfp4(m, f, a.device)
     dev = _check_dev(a.qdata, a.scales, a.rec, w1.qdata, w1.scales, w1.rec, h, act.qdata, act.scales, act.rec)
     st_ptr = ctypes.c_void_p(status.data_ptr()) if status is not None else ctypes.c_void_p(0)
     with torch.cuda.device(dev):

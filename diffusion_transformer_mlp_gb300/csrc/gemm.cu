@@ -719,6 +719,36 @@ nvfp4_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base
   return NVFP4_OK;
 }
 
+// CTA pairs of k_fc2_gemm<gated> that are resident at once on the current
+// device (two-CTA clusters at `smem` bytes each: SMs / 2 on a GB300, fewer
+// where the GPCs cannot all hold pairs), cached per device and variant.
+// The persistent grid is sized to this so that no pair waits for a second
+// wave.
+nvfp4_status resident_pairs(bool gated, int smem, int* pairs) {
+  static std::mutex mu;
+  static int cache[64][2] = {};
+  int dev = 0;
+  nvfp4_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != NVFP4_OK) return st;
+  if (dev < 0 || dev >= 64) return fail(NVFP4_EUNSUPPORTED, "device ordinal above 63");
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][gated ? 1 : 0];
+  if (c == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    int clusters = 0;
+    st = cuda_check(cudaOccupancyMaxActiveClusters(&clusters, gated ? k_fc2_gemm<true> : k_fc2_gemm<false>, &cfg),
+                    "cudaOccupancyMaxActiveClusters(k_fc2_gemm)");
+    if (st != NVFP4_OK) return st;
+    if (clusters < 1) return fail(NVFP4_ECUDA, "k_fc2_gemm: no two-CTA cluster fits on this device");
+    c = clusters < sm_count() / 2 ? clusters : sm_count() / 2;
+  }
+  *pairs = c;
+  return NVFP4_OK;
+}
+
 }  // namespace
 
 // Default bounded-wait limit in SM cycles (about two seconds at the highest
@@ -833,7 +863,10 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
                   "cudaFuncSetAttribute(k_fc2_gemm)");
   if (st != NVFP4_OK) return st;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
-  const int pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
+  int max_pairs = 0;
+  st = resident_pairs(gated, smem, &max_pairs);
+  if (st != NVFP4_OK) return st;
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
   kernel<<<2 * pairs, THREADS, smem, stream>>>(ta, tw, tsa, tsw, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }

@@ -24,9 +24,9 @@ extern "C" {
 nvfp4_status nvfp4_diag_silu_all(uint16_t* out, nvfp4_stream_t stream);
 
 /* out[g] = BF16 bits of the silu the SwiGLU epilogue of nvfp4_fc1_swiglu
- * computes (binary32 arithmetic, the table near BF16 rounding boundaries)
- * for every BF16 gate g (65536 entries, device); must equal
- * nvfp4_diag_silu_all. */
+ * takes (a shared-memory slice of the producer's table for 2^-10 <= |g| <
+ * 8, g itself for g >= 8, the table in global memory otherwise) for every
+ * BF16 gate g (65536 entries, device); must equal nvfp4_diag_silu_all. */
 nvfp4_status nvfp4_diag_silu_epilogue(uint16_t* out, nvfp4_stream_t stream);
 
 /* h[i] = the producer's SwiGLU output for (gate[i], up[i]), BF16 bits,

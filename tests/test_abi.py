@@ -132,3 +132,39 @@ def test_product_package_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "nvfp4_oracle" not in text, f
+
+
+def _host_nvfp4(rows, cols, qbytes=None, sbytes=None, rec=16):
+    import torch
+    q = torch.zeros(qbytes if qbytes is not None else fc2.qdata_bytes(rows, cols), dtype=torch.uint8)
+    s = torch.zeros(sbytes if sbytes is not None else fc2.scale_bytes(rows, cols), dtype=torch.uint8)
+    return fc2.NVFP4Tensor(q, s, torch.zeros(rec, dtype=torch.uint8), rows, cols)
+
+
+def test_python_wrappers_reject_mismatched_nvfp4_buffers():
+    """A caller-supplied NVFP4Tensor whose shape or byte counts do not fit the
+    call is refused before anything reaches the library (a buffer kept from
+    a smaller M would otherwise receive device writes past its end)."""
+    import torch
+    x = torch.zeros(300, 2 * 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match=r"\[200, 64\]"):
+        fc2.swiglu_nvfp4_quantize(x, out=_host_nvfp4(200, 64))
+    with pytest.raises(ValueError, match="qdata has"):
+        fc2.swiglu_nvfp4_quantize(x, out=_host_nvfp4(300, 64, qbytes=fc2.qdata_bytes(200, 64)))
+    with pytest.raises(ValueError, match="scales has"):
+        fc2.nvfp4_quantize_weight(x, out=_host_nvfp4(300, 128, sbytes=100))
+    with pytest.raises(ValueError, match="rec has"):
+        fc2.nvfp4_quantize_weight(x, out=_host_nvfp4(300, 128, rec=8))
+    a = _host_nvfp4(300, 256)
+    w_small = _host_nvfp4(128, 256, qbytes=128 * 64)
+    with pytest.raises(ValueError, match="w.qdata has"):
+        fc2.nvfp4_fc2_gemm(a, w_small)
+    a_big = fc2.NVFP4Tensor(a.qdata, a.scales, a.rec, 400, 256)  # claims more rows than its buffers hold
+    with pytest.raises(ValueError, match="a.qdata has"):
+        fc2.nvfp4_fc2_gemm(a_big, _host_nvfp4(128, 256))
+    with pytest.raises(ValueError, match="act holds"):
+        fc2.nvfp4_fc1_swiglu(a, _host_nvfp4(256, 256), act=_host_nvfp4(200, 128))
+    strided = fc2.NVFP4Tensor(torch.zeros(2 * fc2.qdata_bytes(300, 256), dtype=torch.uint8)[::2], a.scales,
+                              a.rec, 300, 256)
+    with pytest.raises(ValueError, match="contiguous"):
+        fc2.nvfp4_fc2_gemm(strided, _host_nvfp4(128, 256))

@@ -167,9 +167,10 @@ def test_element_codes_match_correctly_rounded_quotient_everywhere():
 
 
 def test_epilogue_silu_equals_table_for_every_gate():
-    """The SwiGLU epilogue of nvfp4_fc1_swiglu computes silu in binary32 and
-    asks the table only near BF16 rounding boundaries; for all 65,536 gates it
-    must give the table's (correctly rounded) BF16 silu."""
+    """The SwiGLU epilogue of nvfp4_fc1_swiglu reads silu from a 6.5 KB
+    shared-memory slice of the table (2^-10 <= |g| < 8), takes g itself for
+    g >= 8 and reads the table in global memory otherwise; for all 65,536
+    gates it must give the table's (correctly rounded) BF16 silu."""
     L = _lib.load()
     tab = torch.empty(65536, dtype=torch.int16, device="cuda")
     epi = torch.empty(65536, dtype=torch.int16, device="cuda")

@@ -103,11 +103,16 @@ def test_gemm_ragged_m(m):
     rows = sample_rows(m, 1024, seed=0 + 7)
     (ok, worst), _, _ = gemm_check(out0, a_ref, w_ref, rows, n, k)
     assert ok, f"M={m}: worst error / bound = {worst}"
-    out = torch.empty_like(out0)
-    for _ in range(50):
+    # 50 whole steps (producer into the same activation buffers, then the
+    # GEMM) queued back to back on one stream, each into its own output,
+    # with one synchronisation at the end
+    outs = [torch.empty_like(out0) for _ in range(50)]
+    for out in outs:
         fc2.fc2(xd, w_dev, a_dev, out)
-        torch.cuda.synchronize()
-        assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+    torch.cuda.synchronize()
+    for i, out in enumerate(outs):
+        assert torch.equal(out.view(torch.int16), out0.view(torch.int16)), f"run {i}"
+    assert compare_quant(a_dev, *a_ref, m, k) is None
 
 
 def test_gemm_row_invariance_across_m(canonical):
