@@ -49,6 +49,16 @@ def producer_bytes(m, k):
     return 2 * (m * 2 * k * 2) + fc2.qdata_bytes(m, k) + fc2.scale_bytes(m, k)
 
 
+def quant_only_bytes(m, f):
+    """Algorithmic bytes of the two-pass quantiser on a BF16 [m, f] tensor."""
+    import diffusion_transformer_mlp_gb300 as fc2
+    return 2 * (m * f * 2) + fc2.qdata_bytes(m, f) + fc2.scale_bytes(m, f)
+
+
+RAGGED = [37711, 37725, 37742, 37774, 37809, 37838, 37966, 38222]
+QUANT_ONLY_F = [5376, 7168, 14336]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -174,14 +184,46 @@ class OracleTimer:
                 "rows_per_s": 1.0 / per_row}
 
 
-def cpu_baseline():
-    """About 10-30 s of oracle work on a bounded sample (see OracleTimer)."""
-    t = OracleTimer(rows_q=2048, rows_g=32)
-    for _ in range(2):
-        t.step()
-    r = t.result()
-    r.pop("rows_per_s")
-    return r
+def cpu_baseline(x_canon, w_ref, quant_only_inputs):
+    """The oracle, as it stands, on the host cores (one run each):
+    - the SwiGLU producer (SwiGLU + two-pass NVFP4) over the whole canonical
+      gate|up tensor [37810, 2 x 14336]: ms, GB/s of its algorithmic bytes,
+      rows/s;
+    - the quantise-only workload at F = 5376, 7168, 14336 ([37810, F]);
+    - the dequantise-then-FP64 GEMM on the 1,024 seeded rows the parity
+      tests check (seed 7; the first and the last row included), rows/s.
+    `value` is the canonical step's TFLOP/s (2NK per row) at the producer's
+    and the GEMM's measured rates per row."""
+    import numpy as np
+
+    import oracle
+    res = {"kind": "oracle", "cores": oracle.num_threads()}
+    t0 = time.perf_counter()
+    aq, as_, ar = oracle.quantize(x_canon, K, swiglu=True)
+    tp = time.perf_counter() - t0
+    pb = producer_bytes(M, K)
+    res["producer_full"] = {"rows": M, "ms": tp * 1e3, "gbs": pb / tp / 1e9, "rows_per_s": M / tp}
+    qo = {}
+    for f, xq in quant_only_inputs.items():
+        t0 = time.perf_counter()
+        oracle.quantize(xq, f, swiglu=False)
+        t = time.perf_counter() - t0
+        qo[str(f)] = {"ms": t * 1e3, "gbs": quant_only_bytes(M, f) / t / 1e9, "rows_per_s": M / t}
+    res["quantize_only"] = qo
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, M - 1], np.sort(rng.choice(M, size=1024, replace=False))]))
+    wq, ws, wr = w_ref
+    t0 = time.perf_counter()
+    oracle.gemm_rows(aq, as_, ar["global_scale"], wq, ws, wr["global_scale"], N, K, rows)
+    tg = time.perf_counter() - t0
+    res["gemm_rows"] = {"rows": int(rows.size), "ms": tg * 1e3, "rows_per_s": rows.size / tg}
+    per_row = tp / M + tg / rows.size
+    res["value"] = 2 * N * K / per_row / 1e12
+    res["unit"] = "TFLOP/s"
+    res["sample"] = (f"producer on all {M} rows ({tp:.2f} s), quantise-only at F=5376/7168/14336 on all rows, "
+                     f"FP64 GEMM on {rows.size} seeded rows ({tg:.2f} s); value = 2NK x rows/s of the two "
+                     f"per-row rates combined ({1.0 / per_row:.1f} rows/s)")
+    return res
 
 
 def run_reference(args):
@@ -371,6 +413,119 @@ def fc1_and_chain(dev, x, wq2, act2, out2, fp4_peak, loop, reps: int = 20):
                                          "bytes identical to mlp_chain's"}}
 
 
+def _pct(vals, q):
+    v = sorted(vals)
+    return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+
+
+def config_sweep(dev, x_big, w, wq, peaks, fp4_peak, reps: int = 20, ragged_runs: int = 50):
+    """The other workloads of the FC2 spec, each as ms, TFLOP/s or GB/s and
+    a roofline fraction (CUDA events on the launching stream, 3 warm-up runs):
+    - mid: M = 4096 (gate|up = the first 4096 rows of the ragged input, the
+      canonical weight): producer + GEMM;
+    - tiny: M = 256, K = 1024, N = 512 (launch-bound; L2-resident);
+    - quantise-only: nvfp4_quantize_weight on BF16 [37810, F] of the
+      activation law, F = 5376, 7168, 14336;
+    - ragged M: producer + GEMM at each M of the sweep, `ragged_runs` runs
+      back to back with events between them; p50 / p90 of the step and of
+      the GEMM.
+    x_big is gate|up for the largest ragged M; every smaller M uses its
+    first rows (the generator is counter-based, so a prefix is exactly that
+    workload's input)."""
+    import numpy as np
+    import torch
+
+    import diffusion_transformer_mlp_gb300 as fc2
+    import synth
+
+    stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    hbm = peaks["hbm_gbs"]
+
+    def timed(fn, n=reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def step_split(xm, wqm, act, out, n):
+        """n back-to-back producer + GEMM runs; per-run (producer, GEMM) ms."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for _ in range(3):
+            fc2.swiglu_nvfp4_quantize(xm, act, stream)
+            fc2.nvfp4_fc2_gemm(act, wqm, out, status, stream)
+        torch.cuda.synchronize()
+        for e in evs:
+            e[0].record(stream)
+            fc2.swiglu_nvfp4_quantize(xm, act, stream)
+            e[1].record(stream)
+            fc2.nvfp4_fc2_gemm(act, wqm, out, status, stream)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in evs], [e[1].elapsed_time(e[2]) for e in evs]
+
+    res = {}
+    # mid
+    mm = 4096
+    act = fc2.empty_nvfp4(mm, K, dev)
+    out = torch.empty(mm, N, dtype=torch.bfloat16, device=dev)
+    pr, gm = step_split(x_big[:mm], wq, act, out, reps)
+    p_ms, g_ms = statistics.median(pr), statistics.median(gm)
+    tf = 2 * mm * N * K / (g_ms * 1e-3) / 1e12
+    pg = producer_bytes(mm, K) / (p_ms * 1e-3) / 1e9
+    res["mid"] = {"shape": [mm, N, K], "producer_ms": p_ms, "producer_gbs": pg, "producer_frac_of_hbm": pg / hbm,
+                  "gemm_ms": g_ms, "gemm_tflops": tf, "gemm_frac_of_fp4_peak": tf / fp4_peak,
+                  "step_ms": p_ms + g_ms}
+    # tiny
+    mt, kt, nt = 256, 1024, 512
+    xt = torch.from_numpy(synth.activation(mt, kt, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    wt = fc2.nvfp4_quantize_weight(
+        torch.from_numpy(synth.weight(nt, kt, seed=0).view(np.int16)).view(torch.bfloat16).to(dev))
+    act_t = fc2.empty_nvfp4(mt, kt, dev)
+    out_t = torch.empty(mt, nt, dtype=torch.bfloat16, device=dev)
+    pr, gm = step_split(xt, wt, act_t, out_t, reps)
+    p_ms, g_ms = statistics.median(pr), statistics.median(gm)
+    tf = 2 * mt * nt * kt / (g_ms * 1e-3) / 1e12
+    res["tiny"] = {"shape": [mt, nt, kt], "producer_ms": p_ms,
+                   "producer_gbs": producer_bytes(mt, kt) / (p_ms * 1e-3) / 1e9, "gemm_ms": g_ms, "gemm_tflops": tf,
+                   "step_ms": p_ms + g_ms, "note": "launch-bound, inputs L2-resident; reported, not a roofline case"}
+    # quantise-only
+    qo = {}
+    for f in QUANT_ONLY_F:
+        xq = torch.from_numpy(synth.quant_input(M, f, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+        o = fc2.empty_nvfp4(M, f, dev)
+        ms = timed(lambda: fc2.nvfp4_quantize_weight(xq, o, stream))
+        gbs = quant_only_bytes(M, f) / (ms * 1e-3) / 1e9
+        qo[str(f)] = {"shape": [M, f], "ms": ms, "algorithmic_bytes": quant_only_bytes(M, f), "gbs": gbs,
+                      "frac_of_hbm": gbs / hbm}
+        del xq, o
+    res["quantize_only"] = qo
+    # ragged M
+    rg = {}
+    for m in RAGGED:
+        act = fc2.empty_nvfp4(m, K, dev)
+        out = torch.empty(m, N, dtype=torch.bfloat16, device=dev)
+        pr, gm = step_split(x_big[:m], wq, act, out, ragged_runs)
+        st = [a + b for a, b in zip(pr, gm)]
+        g50 = _pct(gm, 0.5)
+        rg[str(m)] = {"runs": ragged_runs, "step_ms_p50": _pct(st, 0.5), "step_ms_p90": _pct(st, 0.9),
+                      "gemm_ms_p50": g50, "gemm_ms_p90": _pct(gm, 0.9),
+                      "producer_ms_p50": _pct(pr, 0.5), "producer_ms_p90": _pct(pr, 0.9),
+                      "gemm_tflops_p50": 2 * m * N * K / (g50 * 1e-3) / 1e12}
+        del act, out
+    res["ragged_m"] = rg
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status not OK in the configuration sweep")
+    return res
+
+
 def run_ours(args):
     global M
     if args.m is not None:
@@ -393,11 +548,16 @@ def run_ours(args):
     fc2.load()
     peaks = load_peaks()
 
-    # ---- inputs (host synth -> HBM) and buffers
-    x_host = torch.empty(M, 2 * K, dtype=torch.bfloat16).pin_memory()
-    synth.activation(M, K, seed=0, out=x_host.view(torch.int16).numpy().view(np.uint16))
+    # ---- inputs (host synth -> HBM) and buffers.  gate|up is generated for
+    # the largest M the run needs; the canonical input is its first M rows
+    # (the generator is counter-based: a prefix is exactly that workload).
+    m_big = M if args.no_configs else max(M, max(RAGGED))
+    x_big_host = torch.empty(m_big, 2 * K, dtype=torch.bfloat16).pin_memory()
+    synth.activation(m_big, K, seed=0, out=x_big_host.view(torch.int16).numpy().view(np.uint16))
+    x_host = x_big_host[:M]
     w_host = synth.weight(N, K, seed=0)
-    x = x_host.to(dev)
+    x_big = x_big_host.to(dev)
+    x = x_big[:M]
     w = torch.from_numpy(w_host.view(np.int16)).view(torch.bfloat16).to(dev)
     wq = fc2.empty_nvfp4(N, K, dev)
     act = fc2.empty_nvfp4(M, K, dev)
@@ -518,6 +678,7 @@ def run_ours(args):
     fp4_peak = peaks["bf16_tflops"] * 6.0  # dense FP4 / BF16 nominal ratio 13.5 / 2.25
     loop = None if args.no_mma_loop else fp4_mma_loop(dev, uuid)
     extra = None if args.no_fc1 else fc1_and_chain(dev, x, wq, act, out, fp4_peak, loop)
+    configs = None if args.no_configs else config_sweep(dev, x_big, w, wq, peaks, fp4_peak)
     pbytes = producer_bytes(M, K)
     if not e2e_steps:
         e2e = None
@@ -552,14 +713,17 @@ def run_ours(args):
                 "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": f"replicas x{world}",
                            "l2": "inputs larger than L2 (gate|up 2.17 GB per step), no flush"},
                 "gemm_tflops": gemm_tflops, "producer_ms": prod_ms, "weight_quant_ms": wq_ms, "gemm_ms": gemm_ms,
-                "kernels": kernels, "roofline": roofline, "clocks": clocks, "e2e": e2e,
+                "kernels": kernels, "configs": configs, "roofline": roofline, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": 5 * args.steps,
                 "baseline_context": {"pages_gb10_producer_plus_fc2_ms": PAGES_STEP_MS,
                                      "pages_gb10_tflops": PAGES_TFLOPS}}
         if args.m is not None:
             line["config"]["note"] = f"M overridden to {M}: a profiling case, not the canonical workload"
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            import oracle
+            qo_inputs = {f: synth.quant_input(M, f, seed=0) for f in QUANT_ONLY_F}
+            line["cpu_baseline"] = cpu_baseline(x_host.view(torch.int16).numpy().view(np.uint16), 
+                                                oracle.quantize(w_host, K, swiglu=False), qo_inputs)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -576,6 +740,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-mma-loop", action="store_true", help="skip the in-repo dense FP4 tensor-core loop")
     ap.add_argument("--no-fc1", action="store_true", help="skip the FC1 GEMM and FC1 -> producer -> FC2 chain")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the mid / tiny / quantise-only / ragged-M measurements")
     ap.add_argument("--m", type=int, default=None,
                     help="override M (smaller cases for ncu captures; not a bench line)")
     args = ap.parse_args()

@@ -37,3 +37,19 @@ def test_traffic_record_entries_name_existing_sources():
         assert os.path.exists(src)
         assert rec[key]["bytes_per_launch"] > 0
         assert len(rec[key]["source_sha256_16"]) == 16
+
+
+def test_quantize_only_bytes_and_percentiles():
+    """The quantise-only workload's algorithmic bytes (two reads of the BF16
+    input, QDATA and scales written once) and the percentile helper of the
+    ragged-M report."""
+    b = _bench()
+    m, f = 37810, 5376
+    assert b.quant_only_bytes(m, f) == 2 * m * f * 2 + 37888 * f // 2 + 37888 * (f // 16)
+    # the SwiGLU producer writes the same NVFP4 bytes and reads twice the BF16
+    # input (gate and up) in each of its two passes
+    k = 14336
+    assert b.producer_bytes(m, k) - 2 * (m * 2 * k * 2) == b.quant_only_bytes(m, k) - 2 * (m * k * 2)
+    vals = list(range(1, 51))
+    # nearest rank on the sorted runs: index round(q (n - 1))
+    assert b._pct(vals, 0.5) == 25 and b._pct(vals, 0.9) == 45 and b._pct([3.0], 0.9) == 3.0
