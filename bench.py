@@ -671,7 +671,8 @@ def run_ours(args):
     e2e = {"value": job_throughput(world, FLOP, e2e_s), "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": M * N * 2,
            "steps": e2e_steps, "host_link_measured": link,
-           "api": "nvfp4_quantize_weight + fc2_host(sync=False), two slots (pinned host gate|up in, host BF16 out)"}
+           "api": "nvfp4_quantize_weight + nvfp4_fc2_host (the C ABI's host-to-host step, called through "
+                  "fc2_host(sync=False)), two slots (pinned host gate|up in, host BF16 out)"}
 
     # ---- roofline of the dominant kernel
     gemm_tflops = FLOP / (gemm_ms * 1e-3) / 1e12

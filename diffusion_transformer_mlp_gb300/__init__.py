@@ -204,32 +204,44 @@ def fc2(gate_up: torch.Tensor, w: NVFP4Tensor, act: NVFP4Tensor | None = None, o
 
 def fc2_host(gate_up_host: torch.Tensor, w: NVFP4Tensor, workspace: dict | None = None, stream=None,
              out_host: torch.Tensor | None = None, sync: bool = True):
-    """FC2 from host memory to host memory: copy gate|up to the device, run
-    the step, copy the BF16 output back.  Pinned host tensors make the copies
-    asynchronous; `workspace` (a dict) keeps device buffers between calls.
+    """FC2 from host memory to host memory through nvfp4_fc2_host: the C call
+    copies gate|up to the device, runs the step and copies the BF16 output
+    back, all on `stream`.  Pinned host tensors make the copies
+    asynchronous; `workspace` (a dict) keeps the device buffers between
+    calls.
 
     With ``sync=False`` the call returns ``(out_host, event)`` as soon as the
     work is queued on `stream`; `out_host` is valid, and `workspace` and
     `gate_up_host` may be reused, once `event` has completed.  Two workspaces
     on two streams let one step's copies overlap another step's kernels."""
+    _bf16_matrix(gate_up_host, "gate_up_host")
+    if gate_up_host.device.type != "cpu":
+        raise ValueError("gate_up_host must be a host tensor")
     m, two_k = gate_up_host.shape
     k = two_k // 2
+    n = w.rows
+    _check_nvfp4(w, n, k, "w")
     ws = workspace if workspace is not None else {}
     dev = w.device
-    key = (m, k, w.rows)
+    key = (m, k, n)
     if ws.get("key") != key:
         ws.clear()
         ws["key"] = key
         ws["x"] = torch.empty(m, two_k, dtype=torch.bfloat16, device=dev)
         ws["act"] = empty_nvfp4(m, k, dev)
-        ws["out"] = torch.empty(m, w.rows, dtype=torch.bfloat16, device=dev)
+        ws["out"] = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    if out_host is None:
+        out_host = torch.empty(m, n, dtype=torch.bfloat16, pin_memory=True)
+    if (out_host.dtype != torch.bfloat16 or out_host.device.type != "cpu" or tuple(out_host.shape) != (m, n)
+            or not out_host.is_contiguous()):
+        raise ValueError("out_host must be a contiguous host bfloat16 [m, n] tensor")
     s = torch.cuda.current_stream(dev) if stream is None else stream
-    with torch.cuda.stream(s):
-        ws["x"].copy_(gate_up_host, non_blocking=True)
-        fc2(ws["x"], w, ws["act"], ws["out"], s)
-        if out_host is None:
-            out_host = torch.empty(m, w.rows, dtype=torch.bfloat16, pin_memory=True)
-        out_host.copy_(ws["out"], non_blocking=True)
+    act = ws["act"]
+    with torch.cuda.device(dev):
+        _lib.check(load().nvfp4_fc2_host(_ptr(gate_up_host), m, k, gate_up_host.stride(0), _ptr(w.qdata),
+                                         _ptr(w.scales), _ptr(w.rec), n, _ptr(ws["x"]), _ptr(act.qdata),
+                                         _ptr(act.scales), _ptr(act.rec), _ptr(ws["out"]), _ptr(out_host),
+                                         ctypes.c_void_p(0), ctypes.c_void_p(s.cuda_stream)), "nvfp4_fc2_host")
     if sync:
         s.synchronize()
         return out_host

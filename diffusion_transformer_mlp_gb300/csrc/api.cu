@@ -68,3 +68,36 @@ extern "C" int64_t nvfp4_scale_offset(int64_t r, int64_t c, int64_t cols) {
 extern "C" const char* nvfp4_last_error(void) { return nvfp4::g_last_error.c_str(); }
 
 extern "C" uint32_t nvfp4_version(void) { return (1u << 16) | 0u; }
+
+extern "C" nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int64_t k, int64_t ld_host,
+                                       const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec, int64_t n,
+                                       void* x_dev, void* a_q, void* a_s, nvfp4_scale_rec* a_rec, void* out_dev,
+                                       void* out_host, uint32_t* dev_status, nvfp4_stream_t stream) {
+  using nvfp4::cuda_check;
+  using nvfp4::fail;
+  using nvfp4::aligned16;
+  // Every argument is checked before the first copy is enqueued, so that an
+  // error status still means that nothing was queued.
+  if (!gate_up_host || !w_q || !w_s || !w_rec || !x_dev || !a_q || !a_s || !a_rec || !out_dev || !out_host)
+    return fail(NVFP4_EINVAL, "nvfp4_fc2_host: null pointer");
+  if (m < 1 || k < 1 || n < 1) return fail(NVFP4_EINVAL, "nvfp4_fc2_host: m, k and n must be positive");
+  if (ld_host < 2 * k) return fail(NVFP4_EINVAL, "nvfp4_fc2_host: ld_host must be >= 2k");
+  if (k % 256 != 0 || n % 128 != 0 || nvfp4_padded_rows(m) > (int64_t(1) << 30) || n > (int64_t(1) << 24) ||
+      k > (int64_t(1) << 24))
+    return fail(NVFP4_EUNSUPPORTED, "nvfp4_fc2_host: k must be a multiple of 256 and n of 128 (or too large)");
+  if (!aligned16(x_dev) || !aligned16(a_q) || !aligned16(a_s) || !aligned16(a_rec) || !aligned16(out_dev) ||
+      !aligned16(w_q) || !aligned16(w_s) || !aligned16(w_rec))
+    return fail(NVFP4_EALIGN, "nvfp4_fc2_host: device pointers must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t row_bytes = static_cast<size_t>(2 * k) * 2;
+  nvfp4_status st = cuda_check(cudaMemcpy2DAsync(x_dev, row_bytes, gate_up_host, static_cast<size_t>(ld_host) * 2,
+                                                  row_bytes, static_cast<size_t>(m), cudaMemcpyHostToDevice, s),
+                               "nvfp4_fc2_host: copy of gate|up to the device");
+  if (st != NVFP4_OK) return st;
+  if ((st = swiglu_nvfp4_quantize(x_dev, m, k, 2 * k, a_q, a_s, a_rec, stream)) != NVFP4_OK) return st;
+  if ((st = nvfp4_fc2_gemm(a_q, a_s, a_rec, w_q, w_s, w_rec, m, n, k, out_dev, n, dev_status, stream)) != NVFP4_OK)
+    return st;
+  return cuda_check(cudaMemcpyAsync(out_host, out_dev, static_cast<size_t>(m) * static_cast<size_t>(n) * 2,
+                                    cudaMemcpyDeviceToHost, s),
+                    "nvfp4_fc2_host: copy of the output to the host");
+}

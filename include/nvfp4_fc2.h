@@ -167,6 +167,32 @@ nvfp4_status nvfp4_quantize_with_amax(const void* x_bf16, int64_t rows, int64_t 
                                       void* qdata, void* scales, nvfp4_scale_rec* rec,
                                       nvfp4_stream_t stream);
 
+/* One FC2 step from host memory to host memory ("FC2 NVFP4 Scheduling
+ * Results", Production Integration: forward_swiglu = the accepted producer,
+ * then the FC2 GEMM): the host gate|up is copied into the caller's device
+ * buffer, swiglu_nvfp4_quantize and nvfp4_fc2_gemm run on it, and the BF16
+ * output is copied back to host memory.  Everything is enqueued on
+ * `stream`; the host output is valid once the stream has reached this
+ * point (the call itself does not synchronise).  Pinned host memory makes
+ * both copies asynchronous; with pageable memory the runtime copies
+ * synchronously.
+ *   gate_up_host  host BF16 [m, ld_host], ld_host >= 2k
+ *   m >= 1; k, n as for swiglu_nvfp4_quantize and nvfp4_fc2_gemm
+ *   w_q, w_s, w_rec   the NVFP4 weight [n, k] (device)
+ *   x_dev         device BF16 [m, 2k], contiguous: receives the input
+ *   a_q, a_s, a_rec   device NVFP4 activation buffers of [m, k] (sizes as
+ *                 for swiglu_nvfp4_quantize); written
+ *   out_dev       device BF16 [m, n], contiguous: the GEMM output
+ *   out_host      host BF16 [m, n], contiguous: receives the output
+ *   dev_status    as for nvfp4_fc2_gemm
+ * All device buffers belong to the caller; the library allocates nothing.
+ * Every argument is checked before anything is enqueued (the shapes that
+ * nvfp4_fc2_gemm accepts: k % 256 == 0, n % 128 == 0). */
+nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int64_t k, int64_t ld_host, const void* w_q,
+                            const void* w_s, const nvfp4_scale_rec* w_rec, int64_t n, void* x_dev, void* a_q,
+                            void* a_s, nvfp4_scale_rec* a_rec, void* out_dev, void* out_host,
+                            uint32_t* dev_status, nvfp4_stream_t stream);
+
 /* Message describing the last non-zero status returned on this host thread. */
 const char* nvfp4_last_error(void);
 

@@ -168,3 +168,20 @@ def test_python_wrappers_reject_mismatched_nvfp4_buffers():
                               a.rec, 300, 256)
     with pytest.raises(ValueError, match="contiguous"):
         fc2.nvfp4_fc2_gemm(strided, _host_nvfp4(128, 256))
+
+
+def test_host_step_argument_errors():
+    """nvfp4_fc2_host refuses bad arguments before it enqueues anything (no
+    CUDA call is made, so this runs without a GPU)."""
+    L = _lib.load()
+    p = ctypes.c_void_p(16)
+    args = lambda **kw: [kw.get("gu", p), kw.get("m", 256), kw.get("k", 1024), kw.get("ld", 2048), p, p, p,
+                         kw.get("n", 512), kw.get("x", p), p, p, p, p, p, None, None]
+    assert L.nvfp4_fc2_host(*args(gu=None)) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_fc2_host(*args(x=None)) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_fc2_host(*args(m=0)) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_fc2_host(*args(ld=2000)) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_fc2_host(*args(k=1040, ld=2080)) == _lib.NVFP4_EUNSUPPORTED
+    assert L.nvfp4_fc2_host(*args(n=200)) == _lib.NVFP4_EUNSUPPORTED
+    assert L.nvfp4_fc2_host(*args(x=ctypes.c_void_p(24))) == _lib.NVFP4_EALIGN
+    assert "nvfp4_fc2_host" in _lib.last_error()
