@@ -381,17 +381,22 @@ def fc1_and_chain(dev, x, wq2, act2, out2, fp4_peak, loop, reps: int = 20):
     chain_fused_ms = timed(chain_fused)
     if int(status.item()) != 0 or fc2.read_rec(act2)["status"] != 0:
         raise RuntimeError("device status not OK in the fused chain measurement")
-    # the block's other projections on the same kernel and input width:
-    # qkv (N = 21504) and attention_output (N = 5376), K = 5376
+    # the block's other projections on the same kernel: qkv reads the hidden
+    # state (N = 21504 = 3 x 7168, K = 5376); attention_output reads the
+    # 7168-feature attention output (N = 5376, K = 7168; its input stands in
+    # for the attention output: BF16 [M, 7168] of the activation law)
     proj = {}
-    for name, n_p, dst in (("qkv_gemm", 4 * N, x), ("attention_output_gemm", N, out2)):
+    act_ao = fc2.nvfp4_quantize_weight(
+        torch.from_numpy(synth.quant_input(M, 7168, seed=3).view(np.int16)).view(torch.bfloat16).to(dev))
+    for name, act_p, n_p, k_p, dst in (("qkv_gemm", act1, 4 * N, k1, x), ("attention_output_gemm", act_ao, N, 7168, out2)):
         wp = fc2.nvfp4_quantize_weight(
-            torch.from_numpy(synth.weight(n_p, k1, seed=2).view(np.int16)).view(torch.bfloat16).to(dev))
-        p_ms = timed(lambda: fc2.nvfp4_fc2_gemm(act1, wp, dst, status, stream))
-        p_tf = 2 * M * n_p * k1 / (p_ms * 1e-3) / 1e12
-        proj[name] = {"shape": [M, n_p, k1], "ms": p_ms, "tflops": p_tf, "frac_of_fp4_peak": p_tf / fp4_peak,
+            torch.from_numpy(synth.weight(n_p, k_p, seed=2).view(np.int16)).view(torch.bfloat16).to(dev))
+        p_ms = timed(lambda: fc2.nvfp4_fc2_gemm(act_p, wp, dst, status, stream))
+        p_tf = 2 * M * n_p * k_p / (p_ms * 1e-3) / 1e12
+        proj[name] = {"shape": [M, n_p, k_p], "ms": p_ms, "tflops": p_tf, "frac_of_fp4_peak": p_tf / fp4_peak,
                       "frac_of_fp4_mma_loop_burst": p_tf / loop["burst_tflops"] if loop else None}
         del wp
+    del act_ao
     if int(status.item()) != 0:
         raise RuntimeError("device status not OK in the projection measurement")
 

@@ -313,11 +313,13 @@ def test_fc1_swiglu_fused_matches_oracle_canonical_rows():
 
 # The block's other NVFP4 projections on the same kernel.  The pages give
 # their launch grids (296 x 168 and 296 x 42 tiles of 128 x 128): N = 21504
-# for qkv and N = 5376 for attention_output; K is read as the hidden size,
-# 5376 (the pages do not state it; their durations scale with N x 5376).
-@pytest.mark.parametrize("n", [21504, 5376], ids=["qkv", "attention_output"])
-def test_block_projection_sampled_rows(n):
-    m, k = 37810, 5376
+# for qkv and N = 5376 for attention_output.  qkv reads the hidden state
+# (K = 5376; 21504 = 3 x 7168); attention_output reads the 7168-feature
+# attention output ("GB10 component-2 nsys summary", native_pack_validation)
+# and writes the hidden size.
+@pytest.mark.parametrize("n,k", [(21504, 5376), (5376, 7168)], ids=["qkv", "attention_output"])
+def test_block_projection_sampled_rows(n, k):
+    m = 37810
     x = synth.quant_input(m, k, seed=n)
     w = synth.weight(n, k, seed=n)
     a_ref = oracle.quantize(x, k, swiglu=False)
