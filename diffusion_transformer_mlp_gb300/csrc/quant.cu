@@ -88,7 +88,7 @@ struct Slice {
 };
 
 template <bool kSwiglu, bool kStream>
-__device__ __forceinline__ void load_slice(const uint16_t* row, int64_t cols, int64_t c0, Slice& s) {
+__device__ __forceinline__ void load_slice(const uint16_t* row, uint32_t cols, uint32_t c0, Slice& s) {
   const uint4* pg = reinterpret_cast<const uint4*>(row + c0);
   uint4 a, b;
   if constexpr (kStream) {
@@ -145,11 +145,13 @@ __device__ __forceinline__ float slice_bound(const Slice& s) {
 }
 
 // Walks the units (row, segment) of a [rows, cols] grid, grid-strided over
-// warps, without a division in the loop.
+// warps, without a division in the loop.  Indices are 32-bit: the host
+// refuses tensors with 2^31 or more units or padded rows (integer index
+// arithmetic was half of pass 2's instructions in 64 bits).
 struct UnitWalker {
-  int64_t row, seg;
-  int64_t step_rows, step_segs, segs;
-  __device__ UnitWalker(int64_t first, int64_t stride, int64_t segs_) : segs(segs_) {
+  uint32_t row, seg;
+  uint32_t step_rows, step_segs, segs;
+  __device__ UnitWalker(uint32_t first, uint32_t stride, uint32_t segs_) : segs(segs_) {
     row = first / segs;
     seg = first - row * segs;
     step_rows = stride / segs;
@@ -172,25 +174,25 @@ struct UnitWalker {
 // tensor is still in L2 when pass 2 (which walks backwards) starts.
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kSwiglu ? kThreadsAmaxSwiglu : kThreadsWeight)
-    k_amax(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, nvfp4_scale_rec* rec) {
+    k_amax(const uint16_t* __restrict__ x, uint32_t rows, uint32_t cols, uint32_t ld, nvfp4_scale_rec* rec) {
   extern __shared__ __align__(16) uint16_t tab[];
   __shared__ uint32_t wmax[32];
   load_table<kSwiglu>(tab);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int64_t segs = (cols + kSegElems - 1) / kSegElems;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
+  const uint32_t segs = (cols + kSegElems - 1) / kSegElems;
+  const uint32_t first = blockIdx.x * uint32_t(nwarps) + uint32_t(warp);
+  const uint32_t stride = gridDim.x * uint32_t(nwarps);
   uint32_t amax = 0;  // bit pattern of the exact max |h| this lane has evaluated
   UnitWalker w(first, stride, segs);
   while (w.row < rows) {
-    const int64_t r0 = w.row, c0 = w.seg * kSegElems + lane * 16;
+    const uint32_t r0 = w.row, c0 = w.seg * kSegElems + lane * 16;
     w.next();
-    const int64_t r1 = w.row, c1 = w.seg * kSegElems + lane * 16;
+    const uint32_t r1 = w.row, c1 = w.seg * kSegElems + lane * 16;
     w.next();
     Slice s0, s1;
     const bool v0 = c0 < cols, v1 = r1 < rows && c1 < cols;
-    if (v0) load_slice<kSwiglu, false>(x + r0 * ld, cols, c0, s0);
-    if (v1) load_slice<kSwiglu, false>(x + r1 * ld, cols, c1, s1);
+    if (v0) load_slice<kSwiglu, false>(x + uint64_t(r0) * ld, cols, c0, s0);
+    if (v1) load_slice<kSwiglu, false>(x + uint64_t(r1) * ld, cols, c1, s1);
     if constexpr (kSwiglu) {
       // exact evaluation only where the bound could beat the running max
       if (v0 && !(slice_bound(s0) <= __uint_as_float(amax))) amax = max(amax, slice_absmax_bits<true>(s0, tab));
@@ -307,7 +309,7 @@ __device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float 
 // left in L2; rows >= rows are zeros.
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight)
-    k_quant(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int64_t rows_pad,
+    k_quant(const uint16_t* __restrict__ x, uint32_t rows, uint32_t cols, uint32_t ld, uint32_t rows_pad,
             uint8_t* __restrict__ qdata, uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
   extern __shared__ __align__(16) uint16_t tab[];
   load_table<kSwiglu>(tab);
@@ -324,24 +326,24 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
     rec->status = finite ? NVFP4_OK : NVFP4_ENONFINITE;
   }
 
-  const int64_t segs = (cols + kSegElems - 1) / kSegElems;
-  const int64_t cpad4 = (cols / 16 + 3) / 4;  // 4-column scale groups per row
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
+  const uint32_t segs = (cols + kSegElems - 1) / kSegElems;
+  const uint32_t cpad4 = (cols / 16 + 3) / 4;  // 4-column scale groups per row
+  const uint32_t first = blockIdx.x * uint32_t(nwarps) + uint32_t(warp);
+  const uint32_t stride = gridDim.x * uint32_t(nwarps);
   // Software pipeline: the loads of the next unit are issued before the
   // current one is computed, so a warp keeps its loads in flight while it
   // works (pass 2 is otherwise latency bound on them).
   UnitWalker w(first, stride, segs);
-  int64_t r_n = rows_pad - 1 - w.row, seg_n = segs - 1 - w.seg;
+  uint32_t r_n = rows_pad - 1 - w.row, seg_n = segs - 1 - w.seg;
   bool more = w.row < rows_pad;
   Slice s_n;
   {
-    const int64_t c0 = seg_n * kSegElems + lane * 16;
-    if (more && c0 < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + r_n * ld, cols, c0, s_n);
+    const uint32_t c0 = seg_n * kSegElems + lane * 16;
+    if (more && c0 < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + uint64_t(r_n) * ld, cols, c0, s_n);
   }
   while (more) {
-    const int64_t r = r_n, seg = seg_n;
-    const int64_t c0 = seg * kSegElems + lane * 16;
+    const uint32_t r = r_n, seg = seg_n;
+    const uint32_t c0 = seg * kSegElems + lane * 16;
     const bool valid = c0 < cols;
     const bool loaded = valid && finite && r < rows;
     const Slice s = s_n;
@@ -350,8 +352,8 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
     r_n = rows_pad - 1 - w.row;
     seg_n = segs - 1 - w.seg;
     {
-      const int64_t c0n = seg_n * kSegElems + lane * 16;
-      if (more && c0n < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + r_n * ld, cols, c0n, s_n);
+      const uint32_t c0n = seg_n * kSegElems + lane * 16;
+      if (more && c0n < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + uint64_t(r_n) * ld, cols, c0n, s_n);
     }
     uint32_t hw[8];  // 16 BF16 values of h, two per word
     if (loaded) {
@@ -372,15 +374,15 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
     const float sc = __fmul_rn(e4m3_value(bs), g);
     uint2 packed = make_uint2(0u, 0u);
     if (sc != 0.0f && finite) packed = block_codes(hw, sc, __frcp_rn(sc));
-    if (valid) *reinterpret_cast<uint2*>(qdata + r * (cols / 2) + c0 / 2) = packed;
+    if (valid) *reinterpret_cast<uint2*>(qdata + uint64_t(r) * (cols / 2) + c0 / 2) = packed;
 
     // scales: lanes 4j..4j+3 hold the four blocks of scale group j
     const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
     const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
     const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
-    const int64_t grp = seg * (kSegElems / 64) + (lane >> 2);
+    const uint32_t grp = seg * (kSegElems / 64) + (lane >> 2);
     if ((lane & 3) == 0 && grp < cpad4) {
-      const int64_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+      const uint32_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
       *reinterpret_cast<uint32_t*>(scales + off) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
   }
@@ -411,27 +413,32 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
   if (ld < need) return fail(NVFP4_EINVAL, std::string(name) + ": ld too small");
   if (ld % 8 != 0 || !aligned16(x) || !aligned16(qdata) || !aligned16(scales) || !aligned16(rec))
     return fail(NVFP4_EALIGN, std::string(name) + ": pointers must be 16-byte aligned and ld a multiple of 8");
-  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 30))
-    return fail(NVFP4_EUNSUPPORTED, std::string(name) + ": tensor too large");
   const int64_t rows_pad = nvfp4_padded_rows(rows);
+  // the kernels index units, rows, columns and scale bytes in 32 bits
+  const int64_t limit = int64_t(1) << 31;
+  if (cols > (int64_t(1) << 30) || ld >= limit || rows_pad >= limit ||
+      rows_pad * ((cols + kSegElems - 1) / kSegElems) >= limit || nvfp4_scale_bytes(rows, cols) >= limit)
+    return fail(NVFP4_EUNSUPPORTED, std::string(name) + ": tensor too large");
+  const uint32_t rows32 = static_cast<uint32_t>(rows), cols32 = static_cast<uint32_t>(cols);
+  const uint32_t ld32 = static_cast<uint32_t>(ld), rows_pad32 = static_cast<uint32_t>(rows_pad);
   const uint16_t* xin = static_cast<const uint16_t*>(x);
   uint8_t* q = static_cast<uint8_t*>(qdata);
   uint8_t* s = static_cast<uint8_t*>(scales);
 
   nvfp4_status st;
   if (given_amax)
-    return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows, cols, ld,
-                                rows_pad, q, s, rec);
+    return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32,
+                                rows_pad32, q, s, rec);
   st = cuda_check(cudaMemsetAsync(rec, 0, sizeof(nvfp4_scale_rec), stream), "memset rec");
   if (st != NVFP4_OK) return st;
   if (swiglu) {
-    if ((st = launch_stream_kernel(k_amax<true>, true, kThreadsAmaxSwiglu, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
+    if ((st = launch_stream_kernel(k_amax<true>, true, kThreadsAmaxSwiglu, stream, "launch k_amax", xin, rows32, cols32, ld32, rec)) != NVFP4_OK)
       return st;
-    return launch_stream_kernel(k_quant<true>, true, kThreadsQuantSwiglu, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
+    return launch_stream_kernel(k_quant<true>, true, kThreadsQuantSwiglu, stream, "launch k_quant", xin, rows32, cols32, ld32, rows_pad32, q, s, rec);
   }
-  if ((st = launch_stream_kernel(k_amax<false>, false, kThreadsWeight, stream, "launch k_amax", xin, rows, cols, ld, rec)) != NVFP4_OK)
+  if ((st = launch_stream_kernel(k_amax<false>, false, kThreadsWeight, stream, "launch k_amax", xin, rows32, cols32, ld32, rec)) != NVFP4_OK)
     return st;
-  return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows, cols, ld, rows_pad, q, s, rec);
+  return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32, rows_pad32, q, s, rec);
 }
 
 // ---- diagnostics: the same device functions on test-chosen inputs ----------
