@@ -89,10 +89,15 @@ extern "C" nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int6
       !aligned16(w_q) || !aligned16(w_s) || !aligned16(w_rec))
     return fail(NVFP4_EALIGN, "nvfp4_fc2_host: device pointers must be 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // packed host rows go as one linear copy (a pitched copy of the same bytes
+  // moves them row by row, measurably slower over the host link)
   const size_t row_bytes = static_cast<size_t>(2 * k) * 2;
-  nvfp4_status st = cuda_check(cudaMemcpy2DAsync(x_dev, row_bytes, gate_up_host, static_cast<size_t>(ld_host) * 2,
-                                                  row_bytes, static_cast<size_t>(m), cudaMemcpyHostToDevice, s),
-                               "nvfp4_fc2_host: copy of gate|up to the device");
+  const cudaError_t ce =
+      ld_host == 2 * k
+          ? cudaMemcpyAsync(x_dev, gate_up_host, row_bytes * static_cast<size_t>(m), cudaMemcpyHostToDevice, s)
+          : cudaMemcpy2DAsync(x_dev, row_bytes, gate_up_host, static_cast<size_t>(ld_host) * 2, row_bytes,
+                              static_cast<size_t>(m), cudaMemcpyHostToDevice, s);
+  nvfp4_status st = cuda_check(ce, "nvfp4_fc2_host: copy of gate|up to the device");
   if (st != NVFP4_OK) return st;
   if ((st = swiglu_nvfp4_quantize(x_dev, m, k, 2 * k, a_q, a_s, a_rec, stream)) != NVFP4_OK) return st;
   if ((st = nvfp4_fc2_gemm(a_q, a_s, a_rec, w_q, w_s, w_rec, m, n, k, out_dev, n, dev_status, stream)) != NVFP4_OK)

@@ -155,6 +155,11 @@ def test_fc2_host_matches_device_step():
     for j in range(2):
         evs[j].synchronize()
         assert torch.equal(outs[j].view(torch.int16), ref.cpu().view(torch.int16))
+    # a host input whose rows are longer than 2k (the copy takes the first 2k)
+    wide = torch.zeros(m, 2 * k + 64, dtype=torch.bfloat16).pin_memory()
+    wide[:, : 2 * k] = x_host
+    got = fc2.fc2_host(wide[:, : 2 * k], wq)
+    assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16))
 
 
 # FC1 on the same kernel: M x (2 * 14336) x 5376.  Its input is the block's
