@@ -736,6 +736,23 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def profile_quantize(args):
+    """A profiling case, not a bench line: nvfp4_quantize_weight four times on a
+    BF16 [M, F] input of the activation law (M from --m, else 37810)."""
+    import numpy as np
+    import torch
+
+    import diffusion_transformer_mlp_gb300 as fc2
+    import synth
+    m, f = (args.m or M), args.profile_quantize
+    x = torch.from_numpy(synth.quant_input(m, f, seed=0).view(np.int16)).view(torch.bfloat16).cuda()
+    o = fc2.empty_nvfp4(m, f)
+    for _ in range(4):
+        fc2.nvfp4_quantize_weight(x, o)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": "quantize", "shape": [m, f], "rec": fc2.read_rec(o)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -750,10 +767,14 @@ def main():
                     help="skip the mid / tiny / quantise-only / ragged-M measurements")
     ap.add_argument("--m", type=int, default=None,
                     help="override M (smaller cases for ncu captures; not a bench line)")
+    ap.add_argument("--profile-quantize", type=int, default=None, metavar="F",
+                    help="profiling case (not a bench line): quantise a BF16 [M, F] input four times")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile_quantize is not None:
+        profile_quantize(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
