@@ -86,6 +86,15 @@ def test_quantizer_argument_errors():
     w = L.nvfp4_quantize_weight
     assert w(P16, 4, 64, 32, P16, P16, P16, NUL) == _lib.NVFP4_EINVAL           # ld < cols
     assert w(P16, 4, 64, 64, P16, P16, P8, NUL) == _lib.NVFP4_EALIGN            # rec misaligned
+    # the kernels index in 32 bits: sizes they cannot address are refused
+    assert w(P16, 1 << 31, 16, 16, P16, P16, P16, NUL) == _lib.NVFP4_EUNSUPPORTED     # padded rows
+    assert w(P16, 1 << 24, 1 << 16, 1 << 16, P16, P16, P16, NUL) == _lib.NVFP4_EUNSUPPORTED  # 2^31 units
+    assert w(P16, 4, 64, 1 << 31, P16, P16, P16, NUL) == _lib.NVFP4_EUNSUPPORTED     # row stride
+    assert w(P16, 4, (1 << 30) + 16, (1 << 30) + 16, P16, P16, P16, NUL) == _lib.NVFP4_EUNSUPPORTED
+    assert "too large" in _lib.last_error()
+    # the binding limit at the FC2 width is the scale array: about 2.4 M rows,
+    # far above the canonical 37,888
+    assert fc2.scale_bytes(2_390_000, 14336) < (1 << 31) <= fc2.scale_bytes(2_400_000, 14336)
 
 
 def test_gemm_argument_errors():
