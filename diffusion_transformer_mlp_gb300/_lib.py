@@ -30,7 +30,7 @@ EXPORTED = ["nvfp4_padded_rows", "nvfp4_qdata_bytes", "nvfp4_scale_bytes", "nvfp
             "nvfp4_version", "nvfp4_diag_silu_all", "nvfp4_diag_swiglu", "nvfp4_diag_code_transitions",
             "nvfp4_diag_wait_timeout", "nvfp4_diag_mma_peak", "nvfp4_diag_mma_peak_pairs",
             "nvfp4_diag_quotient_codes", "nvfp4_fc1_swiglu", "nvfp4_quantize_with_amax",
-            "nvfp4_diag_silu_epilogue", "nvfp4_diag_block_scale_codes", "nvfp4_diag_tc_e2m1_read", "nvfp4_fc2_host"]
+            "nvfp4_diag_silu_epilogue", "nvfp4_diag_block_scale_codes", "nvfp4_diag_tc_e2m1_read", "nvfp4_fc2_host", "nvfp4_fc2_host_noalloc"]
 
 _lock = threading.Lock()
 _lib = None
@@ -98,6 +98,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.nvfp4_diag_tc_e2m1_read.restype = st
         L.nvfp4_fc2_host.restype = st
         L.nvfp4_fc2_host.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.nvfp4_fc2_host_noalloc.restype = st
+        L.nvfp4_fc2_host_noalloc.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, vp, vp]
         L.nvfp4_diag_tc_e2m1_read.argtypes = [vp, vp, vp, vp]
         _lib = L
         return _lib

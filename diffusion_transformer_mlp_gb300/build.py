@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 GEN = os.path.join(BUILD, "gen")
 LIB = os.path.join(BUILD, "libnvfp4fc2.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "mma_peak.cu", "tc_read.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "mma_peak.cu", "tc_read.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",
                      "-prec-sqrt=true", "-fmad=true", "-Xptxas", "-v"]

@@ -193,6 +193,33 @@ nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int64_t k, int6
                             void* a_s, nvfp4_scale_rec* a_rec, void* out_dev, void* out_host,
                             uint32_t* dev_status, nvfp4_stream_t stream);
 
+/* nvfp4_fc2_host for callers that cannot allocate device memory.  The pages
+ * have no counterpart: it exists for callers such as a plug-in whose host
+ * program owns the GPU's memory and forbids cudaMalloc, or code that must not
+ * allocate once running (an allocation can block, synchronise the device or
+ * fail under fragmentation).  The step's three device buffers (the copy of
+ * gate|up, the NVFP4 activation, the BF16 output) come from one 32 MiB
+ * (33,554,432-byte) array inside the library, which every GPU that loads the
+ * library holds until the process exits; no cudaMalloc, cudaFree or other
+ * allocating call is made.  The caller still provides the inputs (gate|up in
+ * host memory, the NVFP4 weight on the device) and the host output.
+ *   Arguments as for nvfp4_fc2_host without the device buffers.
+ *   Sizes: 256-byte-rounded m*2k*2 + QDATA + scale bytes + 16 + m*n*2 must
+ *   fit in the 32 MiB, else NVFP4_EUNSUPPORTED with the bytes needed in
+ *   nvfp4_last_error() (FC2 widths, k = 14336 and n = 5376: up to 432 rows;
+ *   the tiny FC2 shape, m = 256, k = 1024, n = 512: 1.4 MiB).  Argument and
+ *   size errors are found before any CUDA call.
+ *   The first call with a device current looks up the array's address on
+ *   that device (cudaGetSymbolAddress, a synchronous runtime call) and keeps
+ *   it; make that first call before any stream capture on the device.
+ *   All calls share the one array and find the last call's bytes in it.
+ *   Nothing in it needs to start at zero (each call writes every byte it
+ *   later reads), but calls whose work overlaps on the GPU (two streams, two
+ *   host threads) race on it: order them on one stream or wait in between. */
+nvfp4_status nvfp4_fc2_host_noalloc(const void* gate_up_host, int64_t m, int64_t k, int64_t ld_host,
+                                    const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec, int64_t n,
+                                    void* out_host, uint32_t* dev_status, nvfp4_stream_t stream);
+
 /* Message describing the last non-zero status returned on this host thread. */
 const char* nvfp4_last_error(void);
 
