@@ -379,8 +379,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ operand producer (both CTAs)
     if (lane == 0) {
+      // the weight and the activation panels in flight are both re-read (the
+      // weight by every M panel, a panel by every N tile of its group): keep
+      // both ahead of the output stores in L2
       const uint64_t pol_w = l2_policy_evict_last();
-      const uint64_t pol_a = l2_policy_evict_normal();
+      const uint64_t pol_a = l2_policy_evict_last();
       Ring r;
       bool ok = true;
       int mt = 0, nt = 0, cur_t = -1;
@@ -410,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ scale producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_last();
-      const uint64_t pol_a = l2_policy_evict_normal();
+      const uint64_t pol_a = l2_policy_evict_last();
       Ring r;
       bool ok = true;
       int mt = 0, nt = 0, cur_t = -1;
@@ -492,6 +495,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int col0 = ((warp - WARP_EPI0) / 4) * (PAIR_N / 2);  // this warp's half of the columns
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
+    // the output is written once and never read back here: evict it first,
+    // so that it does not push the activation panels and the weight out of L2
+    uint64_t pol_out;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_out));
     if constexpr (kGated) {
       // SwiGLU: this warp takes gate columns 64*wh .. +63 and the matching
       // up columns 128 + 64*wh .. +63 of its 32 rows, 32 of each per load
@@ -612,9 +619,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               // scattered 16-byte form cost ~0.065 ms on the canonical case)
 #pragma unroll
               for (int k2 = 0; k2 < 2; ++k2)
-                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * k2), "r"(w[8 * k2]),
+                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(dst + 16 * k2), "r"(w[8 * k2]),
                              "r"(w[8 * k2 + 1]), "r"(w[8 * k2 + 2]), "r"(w[8 * k2 + 3]), "r"(w[8 * k2 + 4]),
-                             "r"(w[8 * k2 + 5]), "r"(w[8 * k2 + 6]), "r"(w[8 * k2 + 7])
+                             "r"(w[8 * k2 + 5]), "r"(w[8 * k2 + 6]), "r"(w[8 * k2 + 7]), "l"(pol_out)
                              : "memory");
             } else {
               uint4* d4 = reinterpret_cast<uint4*>(dst);
