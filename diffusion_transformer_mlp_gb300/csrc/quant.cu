@@ -304,11 +304,12 @@ __device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float 
   return e4m3_code(r);
 }
 
-// Pass 2: quantise.  One lane = one 16-element block.  Units cover rows
+// Pass 2: quantise.  One lane = one 16-element block of each 512-element
+// segment of its unit.  Units cover rows
 // [0, rows_pad), walked from the end so that the first reads hit what pass 1
 // left in L2; rows >= rows are zeros.
-template <bool kSwiglu>
-__global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight)
+template <bool kSwiglu, int kB>
+__global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight, kSwiglu ? 1 : (kB == 2 ? 3 : 4))
     k_quant(const uint16_t* __restrict__ x, uint32_t rows, uint32_t cols, uint32_t ld, uint32_t rows_pad,
             uint8_t* __restrict__ qdata, uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
   extern __shared__ __align__(16) uint16_t tab[];
@@ -326,7 +327,14 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
     rec->status = finite ? NVFP4_OK : NVFP4_ENONFINITE;
   }
 
-  const uint32_t segs = (cols + kSegElems - 1) / kSegElems;
+  // A unit is kB consecutive 512-element segments of one row; lane l owns
+  // the 16-element block 16l of each.  The plain quantiser takes two blocks
+  // a lane on rows that are whole 1024-element units, which halves the
+  // per-unit bookkeeping per element (4-6% faster at 7168 and 14336 columns;
+  // on a row with a partial last unit the idle half cost more than that).
+  static_assert(kB == 1 || (kB == 2 && !kSwiglu), "two blocks a lane for the plain quantiser only");
+  constexpr uint32_t kUnit = kSegElems * kB;
+  const uint32_t segs = (cols + kUnit - 1) / kUnit;
   const uint32_t cpad4 = (cols / 16 + 3) / 4;  // 4-column scale groups per row
   const uint32_t first = blockIdx.x * uint32_t(nwarps) + uint32_t(warp);
   const uint32_t stride = gridDim.x * uint32_t(nwarps);
@@ -336,54 +344,66 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
   UnitWalker w(first, stride, segs);
   uint32_t r_n = rows_pad - 1 - w.row, seg_n = segs - 1 - w.seg;
   bool more = w.row < rows_pad;
-  Slice s_n;
+  Slice s_n[kB];
   {
-    const uint32_t c0 = seg_n * kSegElems + lane * 16;
-    if (more && c0 < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + uint64_t(r_n) * ld, cols, c0, s_n);
+    const uint32_t c0 = seg_n * kUnit + lane * 16;
+#pragma unroll
+    for (int b = 0; b < kB; ++b)
+      if (more && c0 + b * kSegElems < cols && finite && r_n < rows)
+        load_slice<kSwiglu, true>(x + uint64_t(r_n) * ld, cols, c0 + b * kSegElems, s_n[b]);
   }
   while (more) {
     const uint32_t r = r_n, seg = seg_n;
-    const uint32_t c0 = seg * kSegElems + lane * 16;
-    const bool valid = c0 < cols;
-    const bool loaded = valid && finite && r < rows;
-    const Slice s = s_n;
+    const uint32_t c0 = seg * kUnit + lane * 16;
+    Slice s[kB];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) s[b] = s_n[b];
     w.next();
     more = w.row < rows_pad;
     r_n = rows_pad - 1 - w.row;
     seg_n = segs - 1 - w.seg;
     {
-      const uint32_t c0n = seg_n * kSegElems + lane * 16;
-      if (more && c0n < cols && finite && r_n < rows) load_slice<kSwiglu, true>(x + uint64_t(r_n) * ld, cols, c0n, s_n);
+      const uint32_t c0n = seg_n * kUnit + lane * 16;
+#pragma unroll
+      for (int b = 0; b < kB; ++b)
+        if (more && c0n + b * kSegElems < cols && finite && r_n < rows)
+          load_slice<kSwiglu, true>(x + uint64_t(r_n) * ld, cols, c0n + b * kSegElems, s_n[b]);
     }
-    uint32_t hw[8];  // 16 BF16 values of h, two per word
-    if (loaded) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(s.g[i], s.u[i], tab) : s.g[i];
-    } else {
+    for (int b = 0; b < kB; ++b) {
+      const uint32_t cb = c0 + b * kSegElems;
+      const bool valid = cb < cols;
+      const bool loaded = valid && finite && r < rows;
+      uint32_t hw[8];  // 16 BF16 values of h, two per word
+      if (loaded) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hw[i] = 0u;
-    }
-    // |h| max per half; no NaN reaches here (a NaN or Inf anywhere makes the
-    // global max non-finite, and then no element is read)
-    __nv_bfloat162 mh = __floats2bfloat162_rn(0.0f, 0.0f);
+        for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(s[b].g[i], s[b].u[i], tab) : s[b].g[i];
+      } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mh = __hmax2(mh, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&hw[i])));
-    const uint32_t m2 = *reinterpret_cast<const uint32_t*>(&mh);
-    const float bmax = __uint_as_float(max((m2 << 16) & 0x7FFFFFFFu, m2 & 0x7FFF0000u));
-    const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
-    const float sc = __fmul_rn(e4m3_value(bs), g);
-    uint2 packed = make_uint2(0u, 0u);
-    if (sc != 0.0f && finite) packed = block_codes(hw, sc, __frcp_rn(sc));
-    if (valid) *reinterpret_cast<uint2*>(qdata + uint64_t(r) * (cols / 2) + c0 / 2) = packed;
+        for (int i = 0; i < 8; ++i) hw[i] = 0u;
+      }
+      // |h| max per half; no NaN reaches here (a NaN or Inf anywhere makes the
+      // global max non-finite, and then no element is read)
+      __nv_bfloat162 mh = __floats2bfloat162_rn(0.0f, 0.0f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mh = __hmax2(mh, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&hw[i])));
+      const uint32_t m2 = *reinterpret_cast<const uint32_t*>(&mh);
+      const float bmax = __uint_as_float(max((m2 << 16) & 0x7FFFFFFFu, m2 & 0x7FFF0000u));
+      const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
+      const float sc = __fmul_rn(e4m3_value(bs), g);
+      uint2 packed = make_uint2(0u, 0u);
+      if (sc != 0.0f && finite) packed = block_codes(hw, sc, __frcp_rn(sc));
+      if (valid) *reinterpret_cast<uint2*>(qdata + uint64_t(r) * (cols / 2) + cb / 2) = packed;
 
-    // scales: lanes 4j..4j+3 hold the four blocks of scale group j
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
-    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
-    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
-    const uint32_t grp = seg * (kSegElems / 64) + (lane >> 2);
-    if ((lane & 3) == 0 && grp < cpad4) {
-      const uint32_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-      *reinterpret_cast<uint32_t*>(scales + off) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      // scales: lanes 4j..4j+3 hold the four blocks of scale group j
+      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
+      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
+      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
+      const uint32_t grp = cb / 64;  // = (seg * kB + b) * 8 + lane / 4
+      if ((lane & 3) == 0 && grp < cpad4) {
+        const uint32_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+        *reinterpret_cast<uint32_t*>(scales + off) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      }
     }
   }
 }
@@ -425,20 +445,22 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
   uint8_t* q = static_cast<uint8_t*>(qdata);
   uint8_t* s = static_cast<uint8_t*>(scales);
 
+  // the plain pass 2 takes two blocks a lane when the row is whole 1024-element units
+  auto quant_plain = (cols % (2 * kSegElems) == 0) ? k_quant<false, 2> : k_quant<false, 1>;
   nvfp4_status st;
   if (given_amax)
-    return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32,
+    return launch_stream_kernel(quant_plain, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32,
                                 rows_pad32, q, s, rec);
   st = cuda_check(cudaMemsetAsync(rec, 0, sizeof(nvfp4_scale_rec), stream), "memset rec");
   if (st != NVFP4_OK) return st;
   if (swiglu) {
     if ((st = launch_stream_kernel(k_amax<true>, true, kThreadsAmaxSwiglu, stream, "launch k_amax", xin, rows32, cols32, ld32, rec)) != NVFP4_OK)
       return st;
-    return launch_stream_kernel(k_quant<true>, true, kThreadsQuantSwiglu, stream, "launch k_quant", xin, rows32, cols32, ld32, rows_pad32, q, s, rec);
+    return launch_stream_kernel(k_quant<true, 1>, true, kThreadsQuantSwiglu, stream, "launch k_quant", xin, rows32, cols32, ld32, rows_pad32, q, s, rec);
   }
   if ((st = launch_stream_kernel(k_amax<false>, false, kThreadsWeight, stream, "launch k_amax", xin, rows32, cols32, ld32, rec)) != NVFP4_OK)
     return st;
-  return launch_stream_kernel(k_quant<false>, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32, rows_pad32, q, s, rec);
+  return launch_stream_kernel(quant_plain, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32, rows_pad32, q, s, rec);
 }
 
 // ---- diagnostics: the same device functions on test-chosen inputs ----------
