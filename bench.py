@@ -283,6 +283,7 @@ def fp4_mma_loop(dev, uuid, seconds: float = 1.0, iters: int = 65536):
     `burst` is the fastest launch, `sustained` the mean of the second half."""
     import ctypes
 
+    import numpy as np
     import torch
 
     from diffusion_transformer_mlp_gb300 import _lib
@@ -295,21 +296,23 @@ def fp4_mma_loop(dev, uuid, seconds: float = 1.0, iters: int = 65536):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp, stp = ctypes.c_void_p(stream.cuda_stream), ctypes.c_void_p(st.data_ptr())
-    _lib.check(L.nvfp4_diag_mma_peak(iters, stp, sp), "nvfp4_diag_mma_peak")
+    _lib.check(L.nvfp4_diag_mma_peak(iters, stp, None, sp), "nvfp4_diag_mma_peak")
     torch.cuda.synchronize()
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(stream)
-    _lib.check(L.nvfp4_diag_mma_peak(iters, stp, sp), "nvfp4_diag_mma_peak")
+    _lib.check(L.nvfp4_diag_mma_peak(iters, stp, None, sp), "nvfp4_diag_mma_peak")
     c1.record(stream)
     torch.cuda.synchronize()
     n = max(4, min(400, int(seconds / max(c0.elapsed_time(c1) * 1e-3, 1e-4))))
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    # per launch, the first pair's clock record: globaltimer ns and SM cycles
+    clk = torch.zeros(n, 4, dtype=torch.int64, device=dev)
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.2)
     evs[0].record(stream)
     for i in range(n):
-        _lib.check(L.nvfp4_diag_mma_peak(iters, stp, sp), "nvfp4_diag_mma_peak")
+        _lib.check(L.nvfp4_diag_mma_peak(iters, stp, ctypes.c_void_p(clk[i].data_ptr()), sp), "nvfp4_diag_mma_peak")
         evs[i + 1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -317,10 +320,62 @@ def fp4_mma_loop(dev, uuid, seconds: float = 1.0, iters: int = 65536):
         raise RuntimeError("FP4 MMA loop reported a device timeout")
     ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
     tf = [flop / (t * 1e-3) / 1e12 for t in ms]
+    c = clk.cpu().numpy()
+    cyc, ns = c[:, 3] - c[:, 2], c[:, 1] - c[:, 0]
+    in_kernel = {"sm_mhz_median": float(np.median(1e3 * cyc / ns)), "sm_mhz_min": float(np.min(1e3 * cyc / ns)),
+                 "cycles_per_mma_median": float(np.median(cyc / iters)), "cycles_per_mma_min": float(np.min(cyc / iters)),
+                 "source": "globaltimer and clock64 of the first pair, per launch"}
     return {"burst_tflops": max(tf), "sustained_tflops": statistics.mean(tf[n // 2:]), "pairs": pairs,
             "iters_per_launch": iters, "launches": n, "flop_per_launch": flop,
-            "ms_per_launch_mean": statistics.mean(ms), "clocks": clocks,
+            "ms_per_launch_mean": statistics.mean(ms), "clocks": clocks, "in_kernel_clock": in_kernel,
             "kernel": "k_diag_mma_peak (tcgen05.mma.cta_group::2.kind::mxf4nvf4 M256 N256 K64, smem operands)"}
+
+
+def gemm_clock_record(dev, step_parts, act, wq, out, loop, steps: int = 30):
+    """The SM clock the FC2 GEMM runs at and its length in SM cycles:
+    `steps` further steps whose GEMM goes through nvfp4_diag_fc2_gemm_clock
+    (the same kernel; block 0 records globaltimer and clock64 at its start
+    and end).  With the MMA loop's cycles per MMA, the first pair's MMAs
+    give the share of the GEMM's cycles the tensor pipe is busy."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import diffusion_transformer_mlp_gb300 as fc2
+    from diffusion_transformer_mlp_gb300 import _lib
+
+    L = _lib.load()
+    stream = torch.cuda.current_stream(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    clk = torch.zeros(steps, 4, dtype=torch.int64, device=dev)
+    vp = ctypes.c_void_p
+    for i in range(steps):
+        step_parts()
+        _lib.check(L.nvfp4_diag_fc2_gemm_clock(vp(act.qdata.data_ptr()), vp(act.scales.data_ptr()),
+                                               vp(act.rec.data_ptr()), vp(wq.qdata.data_ptr()),
+                                               vp(wq.scales.data_ptr()), vp(wq.rec.data_ptr()), M, N, K,
+                                               vp(out.data_ptr()), N, vp(st.data_ptr()), vp(clk[i].data_ptr()),
+                                               vp(stream.cuda_stream)), "nvfp4_diag_fc2_gemm_clock")
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError("clocked GEMM reported a device timeout")
+    c = clk.cpu().numpy()
+    cyc, ns = c[:, 3] - c[:, 2], c[:, 1] - c[:, 0]
+    res = {"launches": steps, "sm_mhz_median": float(np.median(1e3 * cyc / ns)),
+           "sm_mhz_min": float(np.min(1e3 * cyc / ns)), "sm_mhz_max": float(np.max(1e3 * cyc / ns)),
+           "cycles_median": float(np.median(cyc)), "block0_ms_median": float(np.median(ns)) / 1e6,
+           "source": "globaltimer and clock64 of block 0 (the first pair's leader), per launch"}
+    pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 2
+    tiles = -(-fc2.padded_rows(M) // 256) * (N // 256)
+    pair0_mmas = -(-tiles // pairs) * (K // 64)
+    res["pair0_mmas"] = pair0_mmas
+    if loop and loop.get("in_kernel_clock"):
+        cpm = loop["in_kernel_clock"]["cycles_per_mma_min"]
+        res["tensor_busy_frac"] = pair0_mmas * cpm / res["cycles_median"]
+        res["tensor_busy_note"] = ("first pair's MMAs x the loop's fewest cycles per MMA / the GEMM's cycles "
+                                   f"({pairs} pairs assumed, SMs / 2)")
+    return res
 
 
 def fc1_and_chain(dev, x, wq2, act2, out2, fp4_peak, loop, reps: int = 20):
@@ -683,6 +738,8 @@ def run_ours(args):
     gemm_tflops = FLOP / (gemm_ms * 1e-3) / 1e12
     fp4_peak = peaks["bf16_tflops"] * 6.0  # dense FP4 / BF16 nominal ratio 13.5 / 2.25
     loop = None if args.no_mma_loop else fp4_mma_loop(dev, uuid)
+    clock = gemm_clock_record(dev, lambda: (fc2.nvfp4_quantize_weight(w, wq, stream),
+                                            fc2.swiglu_nvfp4_quantize(x, act, stream)), act, wq, out, loop)
     extra = None if args.no_fc1 else fc1_and_chain(dev, x, wq, act, out, fp4_peak, loop)
     configs = None if args.no_configs else config_sweep(dev, x_big, w, wq, peaks, fp4_peak)
     pbytes = producer_bytes(M, K)
@@ -693,6 +750,7 @@ def run_ours(args):
         "gemm": {"ms": gemm_ms, "tflops": gemm_tflops, "frac_of_fp4_peak": gemm_tflops / fp4_peak,
                  "fp4_mma_loop": loop,
                  "frac_of_fp4_mma_loop_burst": gemm_tflops / loop["burst_tflops"] if loop else None,
+                 "in_kernel_clock": clock,
                  "nvidia_published_dense_fp4_tflops": NVIDIA_DENSE_FP4_TFLOPS},
         "swiglu_producer": {"ms": prod_ms, "algorithmic_bytes": pbytes, "gbs": prod_gbs,
                             "frac_of_hbm": prod_gbs / peaks["hbm_gbs"],

@@ -30,7 +30,8 @@ EXPORTED = ["nvfp4_padded_rows", "nvfp4_qdata_bytes", "nvfp4_scale_bytes", "nvfp
             "nvfp4_version", "nvfp4_diag_silu_all", "nvfp4_diag_swiglu", "nvfp4_diag_code_transitions",
             "nvfp4_diag_wait_timeout", "nvfp4_diag_mma_peak", "nvfp4_diag_mma_peak_pairs",
             "nvfp4_diag_quotient_codes", "nvfp4_fc1_swiglu", "nvfp4_quantize_with_amax",
-            "nvfp4_diag_silu_epilogue", "nvfp4_diag_block_scale_codes", "nvfp4_diag_tc_e2m1_read", "nvfp4_fc2_host", "nvfp4_fc2_host_noalloc"]
+            "nvfp4_diag_silu_epilogue", "nvfp4_diag_block_scale_codes", "nvfp4_diag_tc_e2m1_read", "nvfp4_fc2_host",
+            "nvfp4_fc2_host_noalloc", "nvfp4_diag_fc2_gemm_clock"]
 
 _lock = threading.Lock()
 _lib = None
@@ -82,7 +83,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.nvfp4_diag_wait_timeout.restype = st
         L.nvfp4_diag_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
         L.nvfp4_diag_mma_peak.restype = st
-        L.nvfp4_diag_mma_peak.argtypes = [i64, vp, vp]
+        L.nvfp4_diag_mma_peak.argtypes = [i64, vp, vp, vp]
+        L.nvfp4_diag_fc2_gemm_clock.restype = st
+        L.nvfp4_diag_fc2_gemm_clock.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, vp, vp]
         L.nvfp4_diag_mma_peak_pairs.restype = i64
         L.nvfp4_diag_mma_peak_pairs.argtypes = []
         L.nvfp4_diag_quotient_codes.restype = st

@@ -234,6 +234,9 @@ struct Params {
   // holds both; h = bf16(silu(g) u) goes to out and max |h| to h_rec.
   int f;
   nvfp4_scale_rec* h_rec;
+  // Diagnostic launches only (else null): block 0 writes {start ns, end ns,
+  // start cycle, end cycle} of its run, globaltimer and its SM's clock64.
+  uint64_t* clk;
 };
 
 // Tile order: the N tiles are cut into groups of group_n; a group is walked
@@ -375,6 +378,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated in both
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
+  if (p.clk != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    p.clk[0] = globaltimer_ns();
+    p.clk[2] = clock64();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ operand producer (both CTAs)
@@ -684,6 +691,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   __syncthreads();
   cluster_sync();
   tc_fence_after();
+  if (p.clk != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    p.clk[1] = globaltimer_ns();
+    p.clk[3] = clock64();
+  }
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc_pair(tmem, TMEM_COLS);
@@ -770,7 +781,7 @@ constexpr uint64_t kDefaultWaitLimitCycles = 4000000000ull;
 nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec, const void* w_q,
                          const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m, int64_t n, int64_t k, void* out,
                          int64_t ldo, int64_t f, nvfp4_scale_rec* h_rec, uint32_t* dev_status, cudaStream_t stream,
-                         uint64_t wait_limit_cycles, const char* name) {
+                         uint64_t wait_limit_cycles, const char* name, uint64_t* clk = nullptr) {
   const std::string nm(name);
   const bool gated = f > 0;
   if (!a_q || !a_s || !a_rec || !w_q || !w_s || !w_rec || !out || (gated && !h_rec))
@@ -859,6 +870,7 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   prm.wait_limit_cycles = wait_limit_cycles;
   prm.f = static_cast<int>(f);
   prm.h_rec = h_rec;
+  prm.clk = clk;
   if (gated) {
     st = cuda_check(cudaMemsetAsync(h_rec, 0, sizeof(nvfp4_scale_rec), stream), "memset h_rec");
     if (st != NVFP4_OK) return st;
@@ -925,6 +937,16 @@ extern "C" nvfp4_status nvfp4_fc1_swiglu(const void* a_q, const void* a_s, const
   if (f < 1) return fail(NVFP4_EINVAL, "nvfp4_fc1_swiglu: f must be >= 1");
   return gemm_launch(a_q, a_s, a_rec, w_q, w_s, w_rec, m, 2 * f, k, h_bf16, ldh, f, h_rec, dev_status,
                      reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitCycles, "nvfp4_fc1_swiglu");
+}
+
+extern "C" nvfp4_status nvfp4_diag_fc2_gemm_clock(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec,
+                                                  const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec,
+                                                  int64_t m, int64_t n, int64_t k, void* out_bf16, int64_t ldo,
+                                                  uint32_t* dev_status, uint64_t* clk, nvfp4_stream_t stream) {
+  if (!clk || reinterpret_cast<uintptr_t>(clk) % 8 != 0)
+    return fail(NVFP4_EINVAL, "nvfp4_diag_fc2_gemm_clock: clk must be an 8-byte aligned device pointer");
+  return gemm_launch(a_q, a_s, a_rec, w_q, w_s, w_rec, m, n, k, out_bf16, ldo, 0, nullptr, dev_status,
+                     reinterpret_cast<cudaStream_t>(stream), kDefaultWaitLimitCycles, "nvfp4_diag_fc2_gemm_clock", clk);
 }
 
 extern "C" nvfp4_status nvfp4_diag_wait_timeout(uint64_t limit_ns, uint32_t* dev_status, nvfp4_stream_t stream) {

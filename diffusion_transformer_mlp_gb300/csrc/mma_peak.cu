@@ -47,7 +47,7 @@ __device__ __forceinline__ uint64_t peak_desc(uint32_t saddr) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PEAK_THREADS, 1)
-    k_diag_mma_peak(int64_t iters, uint64_t limit_cycles, uint32_t* dev_status) {
+    k_diag_mma_peak(int64_t iters, uint64_t limit_cycles, uint32_t* dev_status, uint64_t* clk) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t done;
@@ -82,6 +82,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PEAK_THREADS, 1)
   cluster_sync();  // both CTAs' tiles and scales are in place
   tc_fence_after();
   if (rank == 0 && threadIdx.x == 0) {
+    if (clk != nullptr && blockIdx.x == 0) {
+      clk[0] = globaltimer_ns();
+      clk[2] = clock64();
+    }
     const uint64_t a_desc = peak_desc(smem_u32(tiles)), b_desc = peak_desc(smem_u32(tiles + TILE_BYTES));
     for (int64_t i = 0; i < iters; ++i) {
       const uint32_t j = uint32_t(i & 3);  // K=64 slice: 32 bytes into each 128-byte row
@@ -94,6 +98,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PEAK_THREADS, 1)
   if (threadIdx.x == 32) {
     if (!mbar_wait_bounded(&done, 0, limit_cycles, nullptr) && dev_status != nullptr)
       atomicExch(dev_status, static_cast<uint32_t>(NVFP4_ETIMEOUT));
+    if (clk != nullptr && blockIdx.x == 0) {  // the same SM as the start record
+      clk[1] = globaltimer_ns();
+      clk[3] = clock64();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -131,12 +139,15 @@ extern "C" int64_t nvfp4_diag_mma_peak_pairs(void) {
   return mma_peak_pairs(&pairs) == NVFP4_OK ? pairs : -1;
 }
 
-extern "C" nvfp4_status nvfp4_diag_mma_peak(int64_t iters, uint32_t* dev_status, nvfp4_stream_t stream) {
+extern "C" nvfp4_status nvfp4_diag_mma_peak(int64_t iters, uint32_t* dev_status, uint64_t* clk,
+                                            nvfp4_stream_t stream) {
   if (iters < 1 || iters > kMaxIters) return fail(NVFP4_EINVAL, "nvfp4_diag_mma_peak: iters outside 1 .. 2^22");
+  if (reinterpret_cast<uintptr_t>(clk) % 8 != 0)
+    return fail(NVFP4_EINVAL, "nvfp4_diag_mma_peak: clk must be 8-byte aligned");
   int pairs = 0;
   nvfp4_status st = mma_peak_pairs(&pairs);
   if (st != NVFP4_OK) return st;
   k_diag_mma_peak<<<2 * pairs, PEAK_THREADS, PEAK_SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(
-      iters, kPeakWaitLimitCycles, dev_status);
+      iters, kPeakWaitLimitCycles, dev_status, clk);
   return cuda_check(cudaGetLastError(), "launch k_diag_mma_peak");
 }

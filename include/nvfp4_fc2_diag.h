@@ -105,8 +105,26 @@ nvfp4_status nvfp4_diag_tc_e2m1_read(const uint8_t* qdata, float* out, uint32_t*
  * tensor pipe.  The caller times the launch on `stream`: FLOP per launch =
  * P * iters * 8388608.  1 <= iters <= 2^22, else NVFP4_EINVAL.  If the
  * final bounded wait runs out, NVFP4_ETIMEOUT is written to *dev_status
- * (device uint32; may be NULL); the accumulators are discarded. */
-nvfp4_status nvfp4_diag_mma_peak(int64_t iters, uint32_t* dev_status, nvfp4_stream_t stream);
+ * (device uint32; may be NULL); the accumulators are discarded.
+ * clk (device, 8-byte aligned, may be NULL) receives the first pair's
+ * clock record: {globaltimer ns when its first MMA is issued, ns when its
+ * last has completed, the SM's clock64 at those two points}.  Cycles per
+ * MMA = (clk[3] - clk[2]) / iters; the SM clock in MHz =
+ * 1000 * (clk[3] - clk[2]) / (clk[1] - clk[0]). */
+nvfp4_status nvfp4_diag_mma_peak(int64_t iters, uint32_t* dev_status, uint64_t* clk, nvfp4_stream_t stream);
+
+/* nvfp4_fc2_gemm with a clock record: the same kernel and arguments, and
+ * block 0 (the first CTA pair's leader) writes {globaltimer ns after its
+ * prologue, ns at the end of its teardown barrier, its SM's clock64 at both
+ * points} to clk (device, four uint64, 8-byte aligned, else NVFP4_EINVAL).
+ * The kernel's time in SM cycles and the clock it ran at follow as for
+ * nvfp4_diag_mma_peak.  The pages measure their FC2 kernel in wall time
+ * only ("FC2 NVFP4 Scheduling Results", Timing); this record separates the
+ * kernel's cycle count from the SM clock the part chose under its load. */
+nvfp4_status nvfp4_diag_fc2_gemm_clock(const void* a_q, const void* a_s, const nvfp4_scale_rec* a_rec,
+                                       const void* w_q, const void* w_s, const nvfp4_scale_rec* w_rec, int64_t m,
+                                       int64_t n, int64_t k, void* out_bf16, int64_t ldo, uint32_t* dev_status,
+                                       uint64_t* clk, nvfp4_stream_t stream);
 
 /* P above: the SM pairs that hold one two-CTA cluster of the loop each at
  * the same time on the current device (SMs / 2 unless fewer fit); -1 if

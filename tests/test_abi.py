@@ -125,12 +125,18 @@ def test_diag_argument_errors():
     assert L.nvfp4_diag_code_transitions(2, P16, 10, P16, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_wait_timeout(0, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_wait_timeout(10 ** 10, P16, NUL) == _lib.NVFP4_EINVAL
-    assert L.nvfp4_diag_mma_peak(0, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_mma_peak(0, P16, NUL, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_mma_peak(64, P16, ctypes.c_void_p(0x1004), NUL) == _lib.NVFP4_EINVAL  # clk misaligned
     assert L.nvfp4_diag_quotient_codes(1, 0, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_quotient_codes(0x7F80, 1, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_quotient_codes(1, 0x7F80, P16, NUL) == _lib.NVFP4_EINVAL
     assert L.nvfp4_diag_quotient_codes(1, 1, NUL, NUL) == _lib.NVFP4_EINVAL
-    assert L.nvfp4_diag_mma_peak((1 << 22) + 1, P16, NUL) == _lib.NVFP4_EINVAL
+    assert L.nvfp4_diag_mma_peak((1 << 22) + 1, P16, NUL, NUL) == _lib.NVFP4_EINVAL
+    # the clocked GEMM wants its record buffer (checked before any CUDA call)
+    g = L.nvfp4_diag_fc2_gemm_clock
+    assert g(P16, P16, P16, P16, P16, P16, 256, 256, 256, P16, 256, NUL, NUL, NUL) == _lib.NVFP4_EINVAL
+    assert g(P16, P16, P16, P16, P16, P16, 256, 256, 256, P16, 256, NUL, ctypes.c_void_p(0x1004), NUL) == \
+        _lib.NVFP4_EINVAL
 
 
 def test_product_package_does_not_import_oracle():

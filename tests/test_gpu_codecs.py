@@ -125,7 +125,7 @@ def test_fp4_mma_loop_runs_and_scales():
     for iters in (4096, 4096, 65536):
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record()
-        _lib.check(L.nvfp4_diag_mma_peak(iters, _p(st), _stream()), "mma loop")
+        _lib.check(L.nvfp4_diag_mma_peak(iters, _p(st), None, _stream()), "mma loop")
         c1.record()
         torch.cuda.synchronize()
         ms[iters] = c0.elapsed_time(c1)
@@ -134,6 +134,28 @@ def test_fp4_mma_loop_runs_and_scales():
     assert 8.0 < ratio < 20.0, ms
     tflops = pairs * 65536 * 2 * 256 * 256 * 64 / (ms[65536] * 1e-3) / 1e12
     assert 2250.0 < tflops < 30000.0, tflops
+
+
+def test_fp4_mma_loop_clock_record():
+    """The loop's clock record: the first pair's span in SM cycles grows with
+    the MMAs issued, and the SM clock it implies lies between 0.3 and 2.5 GHz
+    (the part's highest clock is 2.07 GHz); cycles per MMA are those of a
+    dense tensor core (an M=256 N=256 K=64 pair MMA is 8.4 MFLOP)."""
+    L = _lib.load()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    clk = torch.zeros(2, 4, dtype=torch.int64, device="cuda")
+    for i, iters in enumerate((4096, 65536)):
+        _lib.check(L.nvfp4_diag_mma_peak(iters, _p(st), _p(clk[i]), _stream()), "mma loop")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    c = clk.cpu().numpy()
+    ns, cyc = c[:, 1] - c[:, 0], c[:, 3] - c[:, 2]
+    assert (ns > 0).all() and (cyc > 0).all(), c
+    mhz = 1e3 * cyc / ns
+    assert ((mhz > 300) & (mhz < 2500)).all(), mhz
+    per_mma = cyc[1] / 65536
+    assert 32 < per_mma < 1024, per_mma
+    assert 8.0 < cyc[1] / cyc[0] < 20.0, cyc
 
 
 def _e4m3_values():

@@ -50,6 +50,34 @@ def test_gemm_mid_all_rows():
     assert ok, f"worst error / bound = {worst}"
 
 
+def test_gemm_clock_record_same_output():
+    """nvfp4_diag_fc2_gemm_clock runs the same kernel: its output equals
+    nvfp4_fc2_gemm's bit for bit, and its clock record is consistent (end
+    after start on both clocks, an SM clock between 0.3 and 2.5 GHz)."""
+    import ctypes
+
+    from diffusion_transformer_mlp_gb300 import _lib
+    m, n, k = 1000, 384, 2048
+    _, _, a_dev, w_dev, _ = build_case(m, n, k, seed=11)
+    ref = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    clk = torch.zeros(4, dtype=torch.int64, device="cuda")
+    vp = ctypes.c_void_p
+    L = _lib.load()
+    _lib.check(L.nvfp4_diag_fc2_gemm_clock(vp(a_dev.qdata.data_ptr()), vp(a_dev.scales.data_ptr()),
+                                           vp(a_dev.rec.data_ptr()), vp(w_dev.qdata.data_ptr()),
+                                           vp(w_dev.scales.data_ptr()), vp(w_dev.rec.data_ptr()), m, n, k,
+                                           vp(out.data_ptr()), n, vp(st.data_ptr()), vp(clk.data_ptr()),
+                                           vp(torch.cuda.current_stream().cuda_stream)), "gemm clock")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    t0, t1, c0, c1 = (int(v) for v in clk.cpu())
+    assert t1 > t0 and c1 > c0
+    assert 300 < 1e3 * (c1 - c0) / (t1 - t0) < 2500
+
+
 def test_gemm_output_bounds_untouched():
     """Rows >= m and columns >= n of a wider output buffer keep their bytes."""
     m, n, k = 130, 256, 512
