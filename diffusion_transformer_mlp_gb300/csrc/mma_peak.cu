@@ -32,7 +32,7 @@ constexpr uint32_t SCALE_W_COL = SCALE_COL + 32;  // W scales: 8 columns per sli
 constexpr int PEAK_SMEM = 160 * 1024;
 static_assert(1024 + 2 * TILE_BYTES <= PEAK_SMEM && 2 * PEAK_SMEM > 233472, "one CTA per SM");
 constexpr uint64_t kPeakWaitLimitCycles = 4000000000ull;  // about 2 s at the highest SM clock
-constexpr int64_t kMaxIters = int64_t(1) << 22;           // at ~140 cycles each, well inside the wait
+constexpr int64_t kMaxIters = int64_t(1) << 22;           // at 128 cycles each, well inside the wait
 
 // kind::mxf4nvf4 instruction descriptor: A and B E2M1 (format 1 at bits 7
 // and 10), both K-major, UE4M3 scales, N/8 at bit 17, M/16 at bit 24.
