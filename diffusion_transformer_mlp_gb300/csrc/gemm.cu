@@ -14,9 +14,10 @@
 //
 //   warp 0      operand TMA producer (both CTAs): per stage KT k-tiles (256
 //               K elements each) of this CTA's 128 A rows and 128 W rows
-//               (128B swizzle) into a STAGES-deep shared-memory ring; the
-//               leader's barrier counts both CTAs' bytes.  A 64 KB stage
-//               takes ~1,800 cycles to land against ~1,100 cycles of MMAs,
+//               (128B swizzle, one box per operand and k-tile) into a
+//               STAGES-deep shared-memory ring; the leader's barriers count
+//               both CTAs' bytes, one barrier per k-tile.  A 64 KB stage
+//               takes ~1,800 cycles to land against ~1,050 cycles of MMAs,
 //               so three stages are in flight.
 //   warp 14     scale TMA producer (both CTAs): per stage this CTA's A
 //               scale blocks and the W scale blocks of both 128-row panels
@@ -31,9 +32,10 @@
 //               would sit in the tensor pipe between the MMAs (a 32x128b
 //               warpx4 copy costs about half an MMA there); tcgen05.st from
 //               other warps does not.
-//   warp 1      MMA issuer (leader CTA): per stage one wait, 4*KT MMAs
-//               reading the operands from the stage and the block scales
-//               from the stage's tensor-memory slot, one commit.
+//   warp 1      MMA issuer (leader CTA): per stage and k-tile one wait and
+//               four MMAs reading the operands from the stage and the block
+//               scales from the stage's tensor-memory slot; one commit per
+//               stage.
 //   warps 2-9   epilogue (both CTAs), two warps per TMEM lane quarter, 128
 //               columns each: tcgen05.ld 32 accumulator columns at a time,
 //               multiply by alpha = gA*gW, round to BF16 and store the
@@ -178,8 +180,9 @@ __device__ __forceinline__ uint32_t swiglu_pair_epi(uint32_t gw, uint32_t uw, co
 struct Smem {
   uint8_t* stage;       // STAGES x [A | B]
   uint8_t* sf;          // SF_RING x [A scales | W scales panel 0 | panel 1]
-  uint64_t* full;       // leader: the operand bytes of both CTAs have landed and
-                        // the stage's scales are in both CTAs' tensor memory
+  uint64_t* full;       // leader: the first k-tile's operand bytes of both CTAs have
+                        // landed and the stage's scales are in both CTAs' tensor memory
+  uint64_t* full_kt1;   // leader: the second k-tile's operand bytes of both CTAs have landed
   uint64_t* empty;      // each CTA: the stage's MMAs are complete (operands and its scale slot free)
   uint64_t* sf_full;    // each CTA: a scale-ring slot has landed
   uint64_t* sf_empty;   // each CTA: the scale writers have read a ring slot
@@ -198,7 +201,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.sf = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.sf + SF_RING * SF_STAGE_BYTES);
   s.full = bars;
-  s.empty = s.full + STAGES;
+  s.full_kt1 = s.full + STAGES;
+  s.empty = s.full_kt1 + STAGES;
   s.sf_full = s.empty + STAGES;
   s.sf_empty = s.sf_full + SF_RING;
   s.tfull = s.sf_empty + SF_RING;
@@ -209,7 +213,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.silu = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + BAR_BYTES);
   return s;
 }
-static_assert((2 * STAGES + 2 * SF_RING + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
+static_assert((3 * STAGES + 2 * SF_RING + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
 static_assert(SMEM_BYTES + kSiluSmemBytes <= 232448, "shared memory budget of the SwiGLU epilogue");
 
 struct Params {
@@ -355,6 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       // the producer's expect_tx arrival plus one per scale writer of either CTA
       mbar_init(&sm.full[s], 1 + 2 * SF_WARPS);
+      mbar_init(&sm.full_kt1[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
     for (int s = 0; s < SF_RING; ++s) {
@@ -399,9 +404,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tile_coords(w.t, p, mt, nt);
           cur_t = w.t;
         }
-        // Boxes beyond the operands (the last M or N half, a k-tile past K)
-        // are zero-filled by the TMA and still count their full bytes, so
-        // every stage carries 2 x STAGE_BYTES for the leader's barrier.
+        // One box per operand and k-tile: the first k-tile of both operands
+        // completes on the stage's barrier, the second on its own, so the
+        // first four MMAs can start while the second k-tile lands.  Boxes
+        // beyond the operands (the last M or N half, a k-tile past K) are
+        // zero-filled by the TMA and still count their full bytes, so each
+        // barrier receives STAGE_BYTES (half a stage from each CTA).
         const int a_row = mt * PAIR_M + int(rank) * HALF;
         const int b_row = kGated ? (rank == 0 ? nt * HALF : p.f + nt * HALF) : nt * PAIR_N + int(rank) * HALF;
         if (!mbar_wait_bounded(&sm.empty[r.slot], r.phase ^ 1u, p.wait_limit_cycles, abort_flag)) {
@@ -411,9 +419,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         uint8_t* st = sm.stage + r.slot * STAGE_BYTES;
         const uint32_t full_leader = mapa_shared(smem_u32(&sm.full[r.slot]), 0);
-        if (leader) mbar_arrive_expect_tx(&sm.full[r.slot], 2 * STAGE_BYTES);
+        const uint32_t kt1_leader = mapa_shared(smem_u32(&sm.full_kt1[r.slot]), 0);
+        if (leader) {
+          mbar_arrive_expect_tx(&sm.full[r.slot], STAGE_BYTES);
+          mbar_arrive_expect_tx(&sm.full_kt1[r.slot], STAGE_BYTES);
+        }
         tma_load_3d_pair(st, &tmap_a, full_leader, 0, a_row, w.ks * KT, pol_a);
         tma_load_3d_pair(st + A_BYTES, &tmap_w, full_leader, 0, b_row, w.ks * KT, pol_w);
+        tma_load_3d_pair(st + KTILE_BYTES, &tmap_a, kt1_leader, 0, a_row, w.ks * KT + 1, pol_a);
+        tma_load_3d_pair(st + A_BYTES + KTILE_BYTES, &tmap_w, kt1_leader, 0, b_row, w.ks * KT + 1, pol_w);
       }
     }
   } else if (warp == WARP_SFP) {
@@ -477,6 +491,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const int kk_end = (ks * KT + KT <= nk) ? KT : nk - ks * KT;
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
+            if (kk == 1) {  // the second k-tile's operands (zeros past K) have landed
+              if (!mbar_wait_bounded(&sm.full_kt1[ab.slot], ab.phase, p.wait_limit_cycles, abort_flag)) {
+                report_timeout(p, sm.abort_flag);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
             if (kk >= kk_end) break;  // the second k-tile of a last stage past K
             const uint64_t a_desc = desc_sw128(st + kk * KTILE_BYTES);
             const uint64_t b_desc = desc_sw128(st + A_BYTES + kk * KTILE_BYTES);
@@ -487,6 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                sf_tmem + SFW_COL + 8 * (4 * kk + j), (ks | kk | j) != 0);
             }
           }
+          if (!ok) break;
           tc_commit_pair(&sm.empty[ab.slot]);  // stage and its scale slot reusable in both CTAs
         }
         if (!ok) break;
@@ -800,8 +823,8 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   if (m_pad > (int64_t(1) << 30) || n > (int64_t(1) << 24) || k > (int64_t(1) << 24))
     return fail(NVFP4_EUNSUPPORTED, nm + ": problem too large");
 
-  // A and W: 3-D views [k-tile][row][128 B] so one box carries KT k-tiles of
-  // 128 rows (each a 128B-swizzled 16 KB tile).  Scales: the A scales as
+  // A and W: 3-D views [k-tile][row][128 B]; one box is one k-tile of 128
+  // rows (a 128B-swizzled 16 KB tile).  Scales: the A scales as
   // [bytes / 256][256] (one 128-row panel x one k-tile is 8 rows = 2 KB),
   // the W scales as [panel][k / 32][256] so one box carries a stage of both
   // panels of a 256-row tile.
@@ -811,7 +834,7 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   {
     const cuuint64_t dims[3] = {128, cuuint64_t(m_pad), cuuint64_t(k / 256)};
     const cuuint64_t strides[2] = {cuuint64_t(k / 2), 128};
-    const cuuint32_t box[3] = {BK_BYTES, HALF, KT};
+    const cuuint32_t box[3] = {BK_BYTES, HALF, 1};
     if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                        "A")) != NVFP4_OK)
       return st;
@@ -819,7 +842,7 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   {
     const cuuint64_t dims[3] = {128, cuuint64_t(n), cuuint64_t(k / 256)};
     const cuuint64_t strides[2] = {cuuint64_t(k / 2), 128};
-    const cuuint32_t box[3] = {BK_BYTES, HALF, KT};
+    const cuuint32_t box[3] = {BK_BYTES, HALF, 1};
     if ((st = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                        "W")) != NVFP4_OK)
       return st;
