@@ -304,6 +304,70 @@ __device__ __forceinline__ uint32_t block_scale_code(float bmax, float d, float 
   return e4m3_code(r);
 }
 
+// One lane's 16-element block of pass 2 at row r, columns cb .. cb+15:
+// `loaded` when the slice holds it (r < rows, inside the columns, finite
+// global max), `valid` when the block lies inside the columns (else nothing
+// is stored).  Writes the packed codes and, from the first lane of each four
+// (one 64-element scale group), the group's scale word.  Every lane of the
+// warp calls it together (the scale word is gathered with shuffles).
+template <bool kSwiglu>
+__device__ __forceinline__ void quant_block(const Slice& sl, bool loaded, bool valid, uint32_t r, uint32_t cb,
+                                            uint32_t cols, uint32_t cpad4, float g, float d, float rd, bool finite,
+                                            const uint16_t* tab, uint8_t* __restrict__ qdata,
+                                            uint8_t* __restrict__ scales, int lane) {
+  uint32_t hw[8];  // 16 BF16 values of h, two per word
+  if (loaded) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(sl.g[i], sl.u[i], tab) : sl.g[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hw[i] = 0u;
+  }
+  // |h| max per half; no NaN reaches here (a NaN or Inf anywhere makes the
+  // global max non-finite, and then no element is read)
+  __nv_bfloat162 mh = __floats2bfloat162_rn(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mh = __hmax2(mh, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&hw[i])));
+  const uint32_t m2 = *reinterpret_cast<const uint32_t*>(&mh);
+  const float bmax = __uint_as_float(max((m2 << 16) & 0x7FFFFFFFu, m2 & 0x7FFF0000u));
+  const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
+  const float sc = __fmul_rn(e4m3_value(bs), g);
+  uint2 packed = make_uint2(0u, 0u);
+  if (sc != 0.0f && finite) packed = block_codes(hw, sc, __frcp_rn(sc));
+  if (valid) *reinterpret_cast<uint2*>(qdata + uint64_t(r) * (cols / 2) + cb / 2) = packed;
+
+  // scales: lanes 4j..4j+3 hold the four blocks of scale group j
+  const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
+  const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
+  const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
+  const uint32_t grp = cb / 64;
+  if ((lane & 3) == 0 && grp < cpad4) {
+    const uint32_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+    *reinterpret_cast<uint32_t*>(scales + off) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+}
+
+// The global scale from pass 1's record (the bit pattern of max |h|); block
+// 0 writes it and the status back to the record.
+struct GlobalScale {
+  bool finite;
+  float g, d, rd;
+};
+
+__device__ __forceinline__ GlobalScale global_scale(nvfp4_scale_rec* rec) {
+  const uint32_t amax_bits = *reinterpret_cast<volatile uint32_t*>(&rec->amax_bits);
+  GlobalScale gs;
+  gs.finite = amax_bits < 0x7F800000u;
+  gs.g = gs.finite ? __fdiv_rn(__uint_as_float(amax_bits), 2688.0f) : __uint_as_float(0x7FC00000u);
+  gs.d = __fmul_rn(6.0f, gs.g);
+  gs.rd = (gs.d == 0.0f || !gs.finite) ? 0.0f : __frcp_rn(gs.d);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    rec->global_scale = gs.g;
+    rec->status = gs.finite ? NVFP4_OK : NVFP4_ENONFINITE;
+  }
+  return gs;
+}
+
 // Pass 2: quantise.  One lane = one 16-element block of each 512-element
 // segment of its unit.  Units cover rows
 // [0, rows_pad), walked from the end so that the first reads hit what pass 1
@@ -315,17 +379,8 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
   extern __shared__ __align__(16) uint16_t tab[];
   load_table<kSwiglu>(tab);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-
-  // Global scale from pass 1's record (the bit pattern of max |h|).
-  const uint32_t amax_bits = *reinterpret_cast<volatile uint32_t*>(&rec->amax_bits);
-  const bool finite = amax_bits < 0x7F800000u;
-  const float g = finite ? __fdiv_rn(__uint_as_float(amax_bits), 2688.0f) : __uint_as_float(0x7FC00000u);
-  const float d = __fmul_rn(6.0f, g);
-  const float rd = (d == 0.0f || !finite) ? 0.0f : __frcp_rn(d);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    rec->global_scale = g;
-    rec->status = finite ? NVFP4_OK : NVFP4_ENONFINITE;
-  }
+  const GlobalScale gs = global_scale(rec);
+  const bool finite = gs.finite;
 
   // A unit is kB consecutive 512-element segments of one row; lane l owns
   // the 16-element block 16l of each.  The plain quantiser takes two blocks
@@ -373,37 +428,83 @@ __global__ void __launch_bounds__(kSwiglu ? kThreadsQuantSwiglu : kThreadsWeight
     for (int b = 0; b < kB; ++b) {
       const uint32_t cb = c0 + b * kSegElems;
       const bool valid = cb < cols;
-      const bool loaded = valid && finite && r < rows;
-      uint32_t hw[8];  // 16 BF16 values of h, two per word
-      if (loaded) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) hw[i] = kSwiglu ? swiglu_pair(s[b].g[i], s[b].u[i], tab) : s[b].g[i];
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) hw[i] = 0u;
-      }
-      // |h| max per half; no NaN reaches here (a NaN or Inf anywhere makes the
-      // global max non-finite, and then no element is read)
-      __nv_bfloat162 mh = __floats2bfloat162_rn(0.0f, 0.0f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mh = __hmax2(mh, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&hw[i])));
-      const uint32_t m2 = *reinterpret_cast<const uint32_t*>(&mh);
-      const float bmax = __uint_as_float(max((m2 << 16) & 0x7FFFFFFFu, m2 & 0x7FFF0000u));
-      const uint32_t bs = finite ? block_scale_code(bmax, d, rd) : 0u;
-      const float sc = __fmul_rn(e4m3_value(bs), g);
-      uint2 packed = make_uint2(0u, 0u);
-      if (sc != 0.0f && finite) packed = block_codes(hw, sc, __frcp_rn(sc));
-      if (valid) *reinterpret_cast<uint2*>(qdata + uint64_t(r) * (cols / 2) + cb / 2) = packed;
+      quant_block<kSwiglu>(s[b], valid && finite && r < rows, valid, r, cb, cols, cpad4, gs.g, gs.d, gs.rd, finite,
+                           tab, qdata, scales, lane);
+    }
+  }
+}
 
-      // scales: lanes 4j..4j+3 hold the four blocks of scale group j
-      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
-      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
-      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
-      const uint32_t grp = cb / 64;  // = (seg * kB + b) * 8 + lane / 4
-      if ((lane & 3) == 0 && grp < cpad4) {
-        const uint32_t off = ((r >> 7) * cpad4 + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-        *reinterpret_cast<uint32_t*>(scales + off) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
-      }
+// Pass 2 of the plain quantiser over the padded [rows_pad, cols] grid read
+// as one sequence of 1024-element units (row-major, so a unit may end in
+// one row and go on in the next).  For cols a multiple of 64 and at least
+// 1024 that are not whole 1024-element units (5376 = 5.25 x 1024): every
+// lane then takes two blocks, where the row walk leaves half a unit of idle
+// lanes at each row end and one block a lane.  A 64-element scale group
+// never straddles two rows (cols % 64 == 0), a unit at most two (cols >=
+// 1024).  Units are walked from the end, as in k_quant.
+__global__ void __launch_bounds__(kThreadsWeight, 3)
+    k_quant_flat(const uint16_t* __restrict__ x, uint32_t rows, uint32_t cols, uint32_t ld, uint32_t rows_pad,
+                 uint8_t* __restrict__ qdata, uint8_t* __restrict__ scales, nvfp4_scale_rec* rec) {
+  constexpr uint32_t kUnit = 2 * kSegElems;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const GlobalScale gs = global_scale(rec);
+  const bool finite = gs.finite;
+  const uint32_t cpad4 = cols / 64;
+  const uint32_t units = uint32_t((uint64_t(rows_pad) * cols) / kUnit);  // exact: rows_pad % 128, cols % 64
+  const uint32_t first = blockIdx.x * uint32_t(nwarps) + uint32_t(warp);
+  const uint32_t stride = gridDim.x * uint32_t(nwarps);
+  // (r, c): the first element of the current unit; stepping back `stride`
+  // units moves it back by dq rows and dr columns (with a borrow).
+  const uint32_t step = stride * kUnit;
+  const uint32_t dq = step / cols, dr = step - dq * cols;
+  uint32_t f = first;
+  uint32_t r = 0, c = 0;
+  if (f < units) {
+    const uint64_t e0 = uint64_t(units - 1 - f) * kUnit;
+    r = uint32_t(e0 / cols);
+    c = uint32_t(e0 - uint64_t(r) * cols);
+  }
+  // this lane's block b of the unit at (r, c): row and column
+  auto block_at = [&](uint32_t ur, uint32_t uc, int b, uint32_t& br, uint32_t& bc) {
+    bc = uc + uint32_t(b) * kSegElems + uint32_t(lane) * 16;
+    br = ur;
+    if (bc >= cols) {
+      bc -= cols;
+      ++br;
+    }
+  };
+  Slice s_n[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    uint32_t br, bc;
+    block_at(r, c, b, br, bc);
+    if (f < units && finite && br < rows) load_slice<false, true>(x + uint64_t(br) * ld, cols, bc, s_n[b]);
+  }
+  while (f < units) {
+    const uint32_t ur = r, uc = c;
+    Slice s[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) s[b] = s_n[b];
+    f += stride;
+    if (c < dr) {
+      c = c + cols - dr;
+      r -= dq + 1;
+    } else {
+      c -= dr;
+      r -= dq;
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      uint32_t br, bc;
+      block_at(r, c, b, br, bc);
+      if (f < units && finite && br < rows) load_slice<false, true>(x + uint64_t(br) * ld, cols, bc, s_n[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      uint32_t br, bc;
+      block_at(ur, uc, b, br, bc);
+      quant_block<false>(s[b], finite && br < rows, true, br, bc, cols, cpad4, gs.g, gs.d, gs.rd, finite, nullptr,
+                         qdata, scales, lane);
     }
   }
 }
@@ -445,8 +546,12 @@ nvfp4_status quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, boo
   uint8_t* q = static_cast<uint8_t*>(qdata);
   uint8_t* s = static_cast<uint8_t*>(scales);
 
-  // the plain pass 2 takes two blocks a lane when the row is whole 1024-element units
-  auto quant_plain = (cols % (2 * kSegElems) == 0) ? k_quant<false, 2> : k_quant<false, 1>;
+  // The plain pass 2 takes two blocks a lane: along each row when it is whole
+  // 1024-element units, else over the grid read as one sequence of units
+  // when cols allows (a multiple of 64, at least 1024), else one block a lane.
+  auto quant_plain = (cols % (2 * kSegElems) == 0)            ? k_quant<false, 2>
+                     : (cols % 64 == 0 && cols >= 2 * kSegElems) ? k_quant_flat
+                                                                 : k_quant<false, 1>;
   nvfp4_status st;
   if (given_amax)
     return launch_stream_kernel(quant_plain, false, kThreadsWeight, stream, "launch k_quant", xin, rows32, cols32, ld32,

@@ -185,7 +185,15 @@ nvfp4_status nvfp4_quantize_with_amax(const void* x_bf16, int64_t rows, int64_t 
  *   out_dev       device BF16 [m, n], contiguous: the GEMM output
  *   out_host      host BF16 [m, n], contiguous: receives the output
  *   dev_status    as for nvfp4_fc2_gemm
- * All device buffers belong to the caller; the library allocates nothing.
+ * All device buffers belong to the caller; the library allocates no device
+ * memory.  The host-to-device copies of all calls on a device run one at a
+ * time in call order: before its copy, `stream` waits for an event that the
+ * library records after the previous call's copy (one CUDA event per device,
+ * created by the first call; the current device must be the stream's).  One
+ * copy at a time keeps the host link, which bounds this step, moving at the
+ * rate of a single copy; callers that pipeline steps on several streams
+ * still overlap one step's copy with another's kernels and output copy.
+ * While `stream` is being captured into a graph the wait is left out.
  * Every argument is checked before anything is enqueued (the shapes that
  * nvfp4_fc2_gemm accepts: k % 256 == 0, n % 128 == 0). */
 nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int64_t k, int64_t ld_host, const void* w_q,
@@ -201,7 +209,7 @@ nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int64_t k, int6
  * gate|up, the NVFP4 activation, the BF16 output) come from one 32 MiB
  * (33,554,432-byte) array inside the library, which every GPU that loads the
  * library holds until the process exits; no cudaMalloc, cudaFree or other
- * allocating call is made.  The caller still provides the inputs (gate|up in
+ * call that allocates device memory is made.  The caller still provides the inputs (gate|up in
  * host memory, the NVFP4 weight on the device) and the host output.
  *   Arguments as for nvfp4_fc2_host without the device buffers.
  *   Sizes: 256-byte-rounded m*2k*2 + QDATA + scale bytes + 16 + m*n*2 must
@@ -211,7 +219,8 @@ nvfp4_status nvfp4_fc2_host(const void* gate_up_host, int64_t m, int64_t k, int6
  *   size errors are found before any CUDA call.
  *   The first call with a device current looks up the array's address on
  *   that device (cudaGetSymbolAddress, a synchronous runtime call) and keeps
- *   it; make that first call before any stream capture on the device.
+ *   it, and nvfp4_fc2_host's first call creates its copy-order event; make
+ *   that first call before any stream capture on the device.
  *   All calls share the one array and find the last call's bytes in it.
  *   Nothing in it needs to start at zero (each call writes every byte it
  *   later reads), but calls whose work overlaps on the GPU (two streams, two

@@ -171,18 +171,26 @@ def test_fc2_host_matches_device_step():
     x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
     got = fc2.fc2_host(x_host, wq)
     assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16))
+    # queued steps on two streams (their host-to-device copies ordered across
+    # the streams by the library), three inputs in turn: every step's output
+    # is checked when its slot comes round again
+    x3 = [x_host] + [torch.from_numpy(synth.activation(m, k, seed=12 + i).view(np.int16)).view(torch.bfloat16)
+                     .pin_memory() for i in range(2)]
+    ref3 = [ref.cpu()] + [fc2.fc2(xi.to("cuda"), wq).cpu() for xi in x3[1:]]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     wss = [{}, {}]
     outs = [torch.empty(m, n, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    evs = [None, None]
-    for i in range(6):
+    evs, last = [None, None], [None, None]
+    for i in range(9):
         j = i % 2
         if evs[j] is not None:
             evs[j].synchronize()
-        _, evs[j] = fc2.fc2_host(x_host, wq, wss[j], streams[j], outs[j], sync=False)
+            assert torch.equal(outs[j].view(torch.int16), ref3[last[j]].view(torch.int16)), (i, j)
+        _, evs[j] = fc2.fc2_host(x3[i % 3], wq, wss[j], streams[j], outs[j], sync=False)
+        last[j] = i % 3
     for j in range(2):
         evs[j].synchronize()
-        assert torch.equal(outs[j].view(torch.int16), ref.cpu().view(torch.int16))
+        assert torch.equal(outs[j].view(torch.int16), ref3[last[j]].view(torch.int16))
     # a host input whose rows are longer than 2k (the copy takes the first 2k)
     wide = torch.zeros(m, 2 * k + 64, dtype=torch.bfloat16).pin_memory()
     wide[:, : 2 * k] = x_host

@@ -33,12 +33,28 @@ def run_swiglu(x: np.ndarray, k: int):
     return dev
 
 
-@pytest.mark.parametrize("rows,cols", [(256, 1024), (1, 16), (300, 1040), (129, 272), (37, 5376), (513, 7168)])
+# Widths for each walk of the plain quantiser's second pass: whole 1024-element
+# units (1024, 7168), multiples of 64 from 1024 up that are not (1088, 1344,
+# 3136, 5376: the grid read as one sequence of units, which crosses row ends),
+# and the rest (16, 272, 1040: one block a lane along each row).
+@pytest.mark.parametrize("rows,cols", [(256, 1024), (1, 16), (300, 1040), (129, 272), (37, 5376), (513, 7168),
+                                       (129, 1088), (1, 1344), (300, 3136), (640, 1344)])
 def test_weight_quantizer_bit_exact_small(rows, cols):
     x = synth.quant_input(rows, cols, seed=rows + cols)
     q, s, rec = oracle.quantize(x, cols, swiglu=False)
     err = compare_quant(run_weight(x, cols), q, s, rec, rows, cols)
     assert err is None, err
+
+
+def test_weight_quantizer_strided_rows_across_row_ends():
+    """The sequence-of-units walk on rows longer than cols (ld > cols): only
+    the first cols columns of each row are read, codes and scales exact."""
+    rows, cols, ld = 200, 1344, 1344 + 192
+    full = synth.quant_input(rows, ld, seed=17)
+    q, s, rec = oracle.quantize(full[:, :cols].copy(), cols, swiglu=False)
+    dev = fc2.nvfp4_quantize_weight(to_dev_bf16(full)[:, :cols])
+    torch.cuda.synchronize()
+    assert compare_quant(dev, q, s, rec, rows, cols) is None
 
 
 @pytest.mark.parametrize("rows,k", [(256, 1024), (1, 16), (300, 1040), (131, 4096), (64, 48)])
