@@ -737,9 +737,11 @@ def run_ours(args):
     # ---- roofline of the dominant kernel
     gemm_tflops = FLOP / (gemm_ms * 1e-3) / 1e12
     fp4_peak = peaks["bf16_tflops"] * 6.0  # dense FP4 / BF16 nominal ratio 13.5 / 2.25
+    # the two clock diagnostics (the MMA loop and the clocked GEMM steps)
     loop = None if args.no_mma_loop else fp4_mma_loop(dev, uuid)
-    clock = gemm_clock_record(dev, lambda: (fc2.nvfp4_quantize_weight(w, wq, stream),
-                                            fc2.swiglu_nvfp4_quantize(x, act, stream)), act, wq, out, loop)
+    clock = None if args.no_mma_loop else gemm_clock_record(
+        dev, lambda: (fc2.nvfp4_quantize_weight(w, wq, stream), fc2.swiglu_nvfp4_quantize(x, act, stream)), act, wq,
+        out, loop)
     extra = None if args.no_fc1 else fc1_and_chain(dev, x, wq, act, out, fp4_peak, loop)
     configs = None if args.no_configs else config_sweep(dev, x_big, w, wq, peaks, fp4_peak)
     pbytes = producer_bytes(M, K)
@@ -819,7 +821,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--no-mma-loop", action="store_true", help="skip the in-repo dense FP4 tensor-core loop")
+    ap.add_argument("--no-mma-loop", action="store_true",
+                    help="skip the in-repo dense FP4 tensor-core loop and the clocked GEMM steps")
     ap.add_argument("--no-fc1", action="store_true", help="skip the FC1 GEMM and FC1 -> producer -> FC2 chain")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the mid / tiny / quantise-only / ragged-M measurements")
