@@ -38,13 +38,16 @@
 //               stage.
 //   warps 2-9   epilogue (both CTAs), two warps per TMEM lane quarter, 128
 //               columns each: tcgen05.ld 32 accumulator columns at a time,
-//               multiply by alpha = gA*gW, round to BF16 and store the
-//               row's 64 bytes straight to global memory as two 32-byte
-//               (whole-sector) stores (rows < M, columns < N); the
-//               accumulator goes back to the MMA issuer after the last
-//               load.  No shared-memory staging: the operand ring needs
-//               the space.  The issuer waits for this drain at every tile
-//               boundary, hence eight warps.
+//               multiply by alpha = gA*gW and round to BF16 into registers;
+//               after the last load the accumulator goes back to the MMA
+//               issuer, and the warp writes its 32 rows x 128 columns
+//               through a 1 KB shared-memory slot, 32 rows x 16 columns at
+//               a time, with TMA stores (which clip rows >= M and columns
+//               >= N).  The issuer waits for the loads at every tile
+//               boundary, hence eight warps; the stores overlap the next
+//               tile's MMAs and leave the load/store unit to the scale
+//               writers.  The SwiGLU epilogue (below) stores h from
+//               registers: its silu slice takes the shared memory.
 //
 // Tiles are walked in groups of N tiles: the whole weight when it fits 48 MB
 // (FC2: all 21 N tiles), else 16 MB of it (21 of FC1's 112); each group is walked
@@ -192,6 +195,7 @@ struct Smem {
   uint32_t* tmem_slot;
   int* abort_flag;
   uint16_t* silu;       // the SwiGLU epilogue's silu entries (k_fc2_gemm<true> only)
+  uint8_t* out_stage;   // the plain epilogue's output slots (k_fc2_gemm<false> only; the same bytes)
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
@@ -211,10 +215,15 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.silu = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + BAR_BYTES);
+  s.out_stage = reinterpret_cast<uint8_t*>(bars) + BAR_BYTES;
   return s;
 }
 static_assert((3 * STAGES + 2 * SF_RING + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
 static_assert(SMEM_BYTES + kSiluSmemBytes <= 232448, "shared memory budget of the SwiGLU epilogue");
+// the plain epilogue's output slots: one per warp, 32 rows x 16 BF16 columns
+constexpr int kOutSlotBytes = 32 * 16 * 2;
+static_assert(SMEM_BYTES + EPI_WARPS * kOutSlotBytes <= 232448, "shared memory budget of the plain epilogue");
+static_assert((SMEM_BYTES - 1024 - BAR_BYTES) % 1024 == 0 && BAR_BYTES % 128 == 0, "output slots 128-byte aligned");
 
 struct Params {
   const nvfp4_scale_rec* a_rec;
@@ -343,7 +352,7 @@ template <bool kGated>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_fc2_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sw,
-               const Params p) {
+               const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -375,6 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_sa);
     prefetch_tmap(&tmap_sw);
+    if constexpr (!kGated) prefetch_tmap(&tmap_out);
   }
   if constexpr (kGated) fill_silu_smem(sm.silu);
   if (warp == 1) tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
@@ -523,6 +533,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int col0 = ((warp - WARP_EPI0) / 4) * (PAIR_N / 2);  // this warp's half of the columns
+    uint8_t* out_slot = sm.out_stage + (warp - WARP_EPI0) * kOutSlotBytes;  // plain epilogue only
     const float alpha = __fmul_rn(p.a_rec->global_scale, p.w_rec->global_scale);
     const uint32_t tempty_leader = mapa_shared(smem_u32(sm.tempty), 0);
     // the output is written once and never read back here: evict it first,
@@ -610,58 +621,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      // Row `lane` of this quarter, columns col0..col0+127, 32 at a time:
-      // TMEM -> registers -> BF16 pairs -> four 16-byte stores (the next
-      // chunk's stores fill the other half of each 32-byte sector).
+      // The warp's 32 rows x 128 columns into registers as BF16 pairs, the
+      // accumulator back to the issuer, then the output through the warp's
+      // shared-memory slot and TMA stores.  Row-per-lane global stores
+      // (32 rows per instruction) held the load/store unit that the scale
+      // writers' ld.shared need: this form took FC2 from 1.496 to 1.447 M
+      // SM cycles and the FC1 shape from 3.601 to 3.284 M.
       const uint32_t row_tmem = tmem + (uint32_t(q * 32) << 16) + ACC_COL + col0;
-      const int row = mt * PAIR_M + int(rank) * HALF + q * 32 + lane;
-      const bool row_ok = row < p.m;
-      __nv_bfloat16* orow = p.out + int64_t(row_ok ? row : 0) * p.ldo + nt * PAIR_N + col0;
-      const int cols = p.n - nt * PAIR_N - col0;  // columns of this half inside N (may be <= 0)
-#pragma unroll 1
-      for (int c2 = 0; c2 < PAIR_N / 128; ++c2) {
-        // two 32-column loads in flight per wait
-        uint32_t r[64];
+      uint32_t wb[4][16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) tmem_ld_32x32b_x32(row_tmem + (2 * c2 + h) * 32, r + 32 * h);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(row_tmem + c * 32, r);
         tc_wait_ld();
-        tmem_ld_fence_regs<64>(r);
-        if (c2 == PAIR_N / 128 - 1) {
-          // accumulator drained: hand it back to the MMA issuer of the pair
-          tc_fence_before();
+        tmem_ld_fence_regs<32>(r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          wb[c][i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha), __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+      }
+      // accumulator drained: hand it back to the MMA issuer of the pair (the
+      // loads are complete: wait::ld, fence::before_thread_sync)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+      // 32 rows x 16 columns per store: lane l writes row l's 32 bytes of
+      // the slot (row-major, as the box lays it out); the next fill waits
+      // until the previous store has read the slot
+      const int y = mt * PAIR_M + int(rank) * HALF + q * 32;
+      const int x0 = nt * PAIR_N + col0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (lane == 0) bulk_wait_read_all();
           __syncwarp();
-          // the loads are complete (wait::ld, fence::before_thread_sync);
-          // a release would also wait for this row's global stores
-          if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 2 * c2 + h;
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = bf16x2_rn(__fmul_rn(__uint_as_float(r[32 * h + 2 * i]), alpha),
-                             __fmul_rn(__uint_as_float(r[32 * h + 2 * i + 1]), alpha));
-          if (row_ok && c * 32 < cols) {
-            __nv_bfloat16* dst = orow + c * 32;
-            if (p.store32) {
-              // two 32-byte stores: each lane writes whole sectors (the
-              // scattered 16-byte form cost ~0.065 ms on the canonical case)
-#pragma unroll
-              for (int k2 = 0; k2 < 2; ++k2)
-                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(dst + 16 * k2), "r"(w[8 * k2]),
-                             "r"(w[8 * k2 + 1]), "r"(w[8 * k2 + 2]), "r"(w[8 * k2 + 3]), "r"(w[8 * k2 + 4]),
-                             "r"(w[8 * k2 + 5]), "r"(w[8 * k2 + 6]), "r"(w[8 * k2 + 7]), "l"(pol_out)
-                             : "memory");
-            } else {
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            }
+          uint4* d = reinterpret_cast<uint4*>(out_slot + lane * 32);
+          d[0] = make_uint4(wb[c][8 * hh], wb[c][8 * hh + 1], wb[c][8 * hh + 2], wb[c][8 * hh + 3]);
+          d[1] = make_uint4(wb[c][8 * hh + 4], wb[c][8 * hh + 5], wb[c][8 * hh + 6], wb[c][8 * hh + 7]);
+          fence_proxy_async_smem();  // the generic-proxy writes, then the TMA's reads
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_out, out_slot, x0 + c * 32 + hh * 16, y, pol_out);
+            bulk_commit();
           }
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // the stores are complete before the CTA exits
     }
   } else {
     // ------------------------------------------------------------ scale writers (both CTAs)
@@ -829,7 +835,7 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   // the W scales as [panel][k / 32][256] so one box carries a stage of both
   // panels of a 256-row tile.
   const int64_t sa_rows = nvfp4_scale_bytes(m, k) / 256;
-  CUtensorMap ta, tw, tsa, tsw;
+  CUtensorMap ta, tw, tsa, tsw, tout;
   nvfp4_status st;
   {
     const cuuint64_t dims[3] = {128, cuuint64_t(m_pad), cuuint64_t(k / 256)};
@@ -861,6 +867,17 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
     const cuuint32_t box[3] = {256, 2 * KSTEPS, gated ? 1u : 2u};
     if ((st = make_map(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_s, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
                        "W scales")) != NVFP4_OK)
+      return st;
+  }
+  {
+    // the output [m, out_cols] BF16, rows ldo apart: one 32-row x 16-column
+    // box per store of the plain epilogue (rows >= m, columns >= out_cols
+    // are clipped by the TMA)
+    const cuuint64_t dims[2] = {cuuint64_t(out_cols), cuuint64_t(m)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldo) * 2};
+    const cuuint32_t box[2] = {16, 32};
+    if ((st = make_map(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       "output")) != NVFP4_OK)
       return st;
   }
   Params prm;
@@ -900,7 +917,7 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   }
 
   auto kernel = gated ? k_fc2_gemm<true> : k_fc2_gemm<false>;
-  const int smem = gated ? SMEM_BYTES + kSiluSmemBytes : SMEM_BYTES;
+  const int smem = gated ? SMEM_BYTES + kSiluSmemBytes : SMEM_BYTES + EPI_WARPS * kOutSlotBytes;
   st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                   "cudaFuncSetAttribute(k_fc2_gemm)");
   if (st != NVFP4_OK) return st;
@@ -909,7 +926,7 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   st = resident_pairs(gated, smem, &max_pairs);
   if (st != NVFP4_OK) return st;
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
-  kernel<<<2 * pairs, THREADS, smem, stream>>>(ta, tw, tsa, tsw, prm);
+  kernel<<<2 * pairs, THREADS, smem, stream>>>(ta, tw, tsa, tsw, tout, prm);
   return cuda_check(cudaGetLastError(), "launch k_fc2_gemm");
 }
 
