@@ -703,10 +703,11 @@ def run_ours(args):
         e2e_step(i)
     for sl in slots:
         sl["ev"].synchronize()
-    # The host link these copies run on, measured on the same buffers (it
-    # differs between machines, e.g. with the NUMA placement of pinned memory).
-    link = {}
-    if e2e_steps:
+    # The host link these copies run on, measured on the same buffers before
+    # and after the timed windows: it differs between machines, and on a
+    # shared host it changes while a run goes on.
+    def host_link():
+        link = {}
         sl = slots[0]
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(sl["stream"]):
@@ -720,17 +721,25 @@ def run_ours(args):
             c1.record(sl["stream"])
             c1.synchronize()
             link["d2h_gbs"] = M * N * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    for sl in slots:
-        sl["ev"].synchronize()
-    e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
-    e2e_s = max_over_ranks(e2e_s, dev)
-    e2e = {"value": job_throughput(world, FLOP, e2e_s), "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+        return link
+
+    link_before = host_link() if e2e_steps else {}
+    # three windows of e2e_steps steps each; the median window is reported
+    windows = []
+    for _ in range(3 if e2e_steps else 0):
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        for sl in slots:
+            sl["ev"].synchronize()
+        windows.append((time.perf_counter() - t0) / e2e_steps)
+    link_after = host_link() if e2e_steps else {}
+    e2e_s = max_over_ranks(statistics.median(windows), dev) if windows else None
+    e2e = None if e2e_s is None else {"value": job_throughput(world, FLOP, e2e_s), "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": M * N * 2,
-           "steps": e2e_steps, "host_link_measured": link,
+           "steps": e2e_steps, "windows_ms_per_step": [w * 1e3 for w in windows],
+           "host_link_measured": {"before": link_before, "after": link_after},
            "api": "nvfp4_quantize_weight + nvfp4_fc2_host (the C ABI's host-to-host step, called through "
                   "fc2_host(sync=False)), two slots (pinned host gate|up in, host BF16 out)"}
 
