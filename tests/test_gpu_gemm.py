@@ -89,6 +89,22 @@ def test_gemm_output_bounds_untouched():
     assert not torch.all(big[:m, :n] == 3.0)
 
 
+def test_gemm_output_view_at_column_offset():
+    """The output as a view that starts 8 columns (16 bytes) into a wider
+    buffer, rows 304 columns apart: the TMA-store epilogue writes the same
+    bytes as into a packed buffer, and nothing outside the view."""
+    m, n, k = 300, 384, 1024
+    _, _, a_dev, w_dev, _ = build_case(m, n, k, seed=21)
+    ref = fc2.nvfp4_fc2_gemm(a_dev, w_dev)
+    big = torch.full((m, n + 304 - n % 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    view = big[:, 8: 8 + n]
+    assert view.data_ptr() % 32 == 16
+    fc2.nvfp4_fc2_gemm(a_dev, w_dev, out=view)
+    torch.cuda.synchronize()
+    assert torch.equal(view.view(torch.int16), ref.view(torch.int16))
+    assert torch.all(big[:, :8] == 7.0) and torch.all(big[:, 8 + n:] == 7.0)
+
+
 def test_gemm_nonfinite_record_propagates_nan():
     m, n, k = 64, 128, 256
     _, _, a_dev, w_dev, xd = build_case(m, n, k, seed=5)
