@@ -232,9 +232,8 @@ struct Params {
   int64_t ldo;
   int store32;       // out is 32-byte aligned and ldo a multiple of 16: 32-byte stores
   int m;             // output rows
-  int a_rows;        // padded rows of the activation (multiple of 128)
   int n;             // weight rows (multiple of 128)
-  int num_m_tiles;   // ceil(a_rows / 256)
+  int num_m_tiles;   // ceil(padded rows of the activation / 256)
   int num_n_tiles;   // ceil(n / 256)
   int group_n;       // N tiles per group of the tile order (see tile_coords)
   int num_k_tiles;   // k / 256
@@ -887,7 +886,6 @@ nvfp4_status gemm_launch(const void* a_q, const void* a_s, const nvfp4_scale_rec
   prm.ldo = ldo;
   prm.store32 = (reinterpret_cast<uintptr_t>(out) % 32 == 0 && ldo % 16 == 0) ? 1 : 0;
   prm.m = static_cast<int>(m);
-  prm.a_rows = static_cast<int>(m_pad);
   prm.n = static_cast<int>(n);
   prm.num_m_tiles = static_cast<int>((m_pad + PAIR_M - 1) / PAIR_M);
   prm.num_n_tiles = static_cast<int>(gated ? f / HALF : (n + PAIR_N - 1) / PAIR_N);
