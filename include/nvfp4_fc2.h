@@ -123,8 +123,10 @@ nvfp4_status swiglu_nvfp4_quantize(const void* gate_up_bf16, int64_t m, int64_t 
  *   a_q, a_s, a_rec   activation QDATA [pad(m), k/2], scales, record (device)
  *   w_q, w_s, w_rec   weight QDATA [n, k/2], scales, record (device)
  *   m >= 1; n >= 128, n % 128 == 0; k >= 256, k % 256 == 0
- *   out_bf16          device [m, ldo] BF16, ldo >= n, ldo % 8 == 0; rows >= m
- *                     and columns >= n are not touched
+ *   out_bf16          device [m, ldo] BF16, 16-byte aligned, ldo >= n,
+ *                     ldo % 8 == 0 (else NVFP4_EALIGN); written by TMA stores
+ *                     through a tensor map of [m, n], so rows >= m and
+ *                     columns >= n are not touched
  *   dev_status        device uint32 or NULL; set to NVFP4_ETIMEOUT if a
  *                     bounded wait ran out (never cleared by the library)
  * No workspace, no atomics; K is reduced in increasing order inside one CTA,
