@@ -124,13 +124,14 @@ def test_edge_blocks_other_global_scales(factor):
     assert err is None, err
 
 
-def test_zero_input_and_nonfinite_status():
-    x = np.zeros((200, 64), dtype=np.uint16)
-    dev = run_weight(x, 64)
+@pytest.mark.parametrize("cols", [64, 1024, 1344])  # one block a lane, two along rows, two across row ends
+def test_zero_input_and_nonfinite_status(cols):
+    x = np.zeros((200, cols), dtype=np.uint16)
+    dev = run_weight(x, cols)
     r = fc2.read_rec(dev)
     assert r["status"] == 0 and r["global_scale"] == 0.0 and not dev.qdata.any() and not dev.scales.any()
     x[150, 17] = 0x7FC0  # NaN
-    dev = run_weight(x, 64)
+    dev = run_weight(x, cols)
     r = fc2.read_rec(dev)
     assert r["status"] == fc2._lib.NVFP4_ENONFINITE and np.isnan(r["global_scale"])
     assert not dev.qdata.any() and not dev.scales.any()
@@ -153,6 +154,23 @@ def test_outputs_fully_overwritten():
     fc2.swiglu_nvfp4_quantize(to_dev_bf16(x), out)
     torch.cuda.synchronize()
     assert compare_quant(out, q, s, rec, rows, k) is None
+
+
+@pytest.mark.parametrize("cols", [48, 1024, 1344])
+def test_plain_outputs_fully_overwritten(cols):
+    """The plain quantiser on each walk writes every QDATA and scale byte of
+    the padded grid (126 pad rows; 48 columns also leave a pad scale column)
+    into buffers pre-filled with 0xAB."""
+    rows = 130
+    x = synth.quant_input(rows, cols, seed=cols)
+    q, s, rec = oracle.quantize(x, cols, swiglu=False)
+    out = fc2.empty_nvfp4(rows, cols)
+    out.qdata.fill_(0xAB)
+    out.scales.fill_(0xAB)
+    out.rec.fill_(0xAB)
+    fc2.nvfp4_quantize_weight(to_dev_bf16(x), out)
+    torch.cuda.synchronize()
+    assert compare_quant(out, q, s, rec, rows, cols) is None
 
 
 @pytest.mark.parametrize("f", [5376, 7168, 14336])
